@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Benchmark of the DFlash draft block attention on GB300.
+
+One step = one pass of the hot path over one batch of synthetic input: a
+``dflash_attn_anchored`` call (validation, anchor-derived tile schedule,
+TMA/tcgen05 attention with online softmax, epilogue) on the bf16 prefill
+workload B=1 H=16 S=4096 nb=256 block_size=16 (Q=4096), d_nope=128, d_rope=64,
+d_v=128, inputs N(0,1).  The metric is TFLOP/s over unmasked FLOPs
+(2*(d_qk+d_v) per visible (query, key, head)).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas, weak scaling); timing is the max over ranks.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dflash_block_draft_gb300 import metrics, synth  # noqa: E402
+
+WORKLOAD = "prefill_bf16"
+METRIC = "DFlash block-attn TFLOP/s (unmasked FLOPs) & % of GB300 bf16 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workload_desc(d) -> str:
+    return (f"{d['workload'].name}: B={d['B']} H={d['H']} S={d['S']} nb={d['nb']} block_size={d['block_size']} "
+            f"Q={d['Q']} d_nope={d['d_nope']} d_rope={d['d_rope']} d_v={d['d_v']} anchored")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (NVML through ctypes; nvidia-smi as fallback)
+# ---------------------------------------------------------------------------
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+            0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+            0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, torch_device_index: int = 0, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []  # (sm_mhz, reasons_mask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._h = None
+        self._smi = None
+        try:
+            import torch
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(torch_device_index).uuid)
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            self._nvml, self._h = nv, h
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._reasons_fn = fn
+        except Exception:
+            self._nvml = None
+
+    def _sample_nvml(self):
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        if self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(mhz)) != 0:
+            return
+        self._reasons_fn(self._h, ctypes.byref(rs))
+        self.samples.append((mhz.value, rs.value))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample_nvml()
+            time.sleep(self.period)
+
+    def start(self):
+        if self._nvml is not None:
+            self._sample_nvml()
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        else:
+            try:
+                self._smi = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "100", "-i", "0"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self._smi = None
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            self._sample_nvml()
+        elif self._smi is not None:
+            self._smi.terminate()
+            out, _ = self._smi.communicate(timeout=5)
+            for line in out.splitlines():
+                try:
+                    a, b, c = [x.strip() for x in line.split(",")]
+                    self.samples.append((int(a), int(c, 16)))
+                    self.max_mhz = int(b)
+                except Exception:
+                    pass
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "unavailable"}
+        mhz = [s[0] for s in self.samples]
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        reasons = [name for bit, name in _REASONS.items() if mask & bit and bit != 0x1]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "source": "nvml" if self._nvml is not None else "nvidia-smi"}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas; the data path has no collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_rows_flops(d, rows):
+    counts = metrics.anchored_visible_counts(d["anchors"], d["S"], d["Q"], d["block_size"]).reshape(-1)
+    return int(counts[rows].sum()) * d["H"] * metrics.flops_per_pair(d["d_nope"], d["d_rope"], d["d_v"])
+
+
+def time_oracle(d, rows):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.anchored(d["q"], d["k_nope"], d["k_rope"], d["v"], d["anchors"], d["block_size"], rows=rows)
+    dt = time.perf_counter() - t0
+    return dt, oracle_rows_flops(d, rows), oracle.max_threads()
+
+
+def cores_available() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    d = synth.make(WORKLOAD)
+    # Each step: every 64th query row of the workload (all heads), ~1.3 GFLOP of oracle work.
+    stride = 64
+    rows = np.arange(0, d["B"] * d["Q"], stride, dtype=np.int64)
+    for _ in range(args.warmup):
+        time_oracle(d, rows)
+    times, flops, threads = [], 0, 1
+    for _ in range(args.steps):
+        dt, fl, threads = time_oracle(d, rows)
+        times.append(dt)
+        flops = fl
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms / 1e3) / 1e12
+    sample = (f"every {stride}th query row of {WORKLOAD} ({rows.size} rows x {d['H']} heads, "
+              f"{flops / 1e9:.2f} GFLOP unmasked per step)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(d), "l2": "n/a (host CPU)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def to_dev(a, dtype, device):
+    import torch
+    a = np.ascontiguousarray(a)
+    if dtype == "bf16":
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(a).to(device)
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    import dflash_block_draft_gb300 as dfl
+    dfl.load_library()
+
+    d = synth.make(WORKLOAD)
+    B, Q, H, S, bs = d["B"], d["Q"], d["H"], d["S"], d["block_size"]
+    dn, dr, dv = d["d_nope"], d["d_rope"], d["d_v"]
+    work = metrics.anchored_work(d["anchors"], S, Q, H, bs, dn, dr, dv, esize=2)
+    host = {k: d[k] for k in ("q", "k_nope", "k_rope", "v")}
+    dev = {k: to_dev(v, "bf16", device) for k, v in host.items()}
+    anchors = torch.from_numpy(d["anchors"]).to(device)
+    out = torch.empty((B, Q, H, dv), dtype=torch.bfloat16, device=device)
+    ws_bytes = dfl.dflash_attn_workspace_size(dfl.MODE_ANCHORED, B, H, S, Q, dn, dr, dv)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 256 MiB > 129 MB L2
+
+    def step():
+        dfl.dflash_attn_anchored(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], anchors, bs, out=out,
+                                 workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    if dfl.dflash_last_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(device.index or 0)
+    launches0 = dfl.dflash_kernel_launches()
+    barrier(world)
+    torch.cuda.synchronize(device)
+    clocks.start()
+    for k in range(args.steps):
+        flush.zero_()  # L2 flushed between timed steps (outside the events)
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clocks.stop()
+    launches = dfl.dflash_kernel_launches() - launches0
+    times = [a.elapsed_time(b) for a, b in ev]
+    ms = max_over_ranks(sum(times) / len(times), world, device)
+    value = world * work["flops"] / (ms / 1e3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    # One kernel per step: the attention kernel is the whole step, so its
+    # average launch duration is the per-step event time.
+    kernel_ms = sum(times) / len(times)
+    achieved = work["flops"] / (kernel_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = load_traffic()
+
+    # end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        pinned = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for k, v in host.items()}
+        an_h = torch.from_numpy(d["anchors"]).pin_memory()
+        out_h = torch.empty((B, Q, H, dv), dtype=torch.bfloat16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values()) + an_h.numel() * 4
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            for k, t in pinned.items():
+                dev[k].copy_(t, non_blocking=True)
+            anchors.copy_(an_h, non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for k in range(args.steps):
+            flush.zero_()
+            ee[k][0].record(stream)
+            e2e_step()
+            ee[k][1].record(stream)
+        torch.cuda.synchronize(device)
+        e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ee) / args.steps, world, device)
+        e2e = {"value": world * work["flops"] / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = np.arange(0, B * Q, 2, dtype=np.int64)  # every other query row, all heads
+        dt, fl, threads = time_oracle(d, rows)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"every 2nd query row of {WORKLOAD} ({rows.size} rows x {H} heads, {fl / 1e9:.1f} GFLOP "
+                         f"unmasked), {dt:.1f} s"}
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_desc(d), "l2": "flushed between timed steps (256 MiB write)",
+                       "unmasked_flops_per_step": work["flops"], "algorithmic_bytes_per_step": work["bytes"],
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic, "peak_source": f"bf16_tflops ({peak_src})",
+                         "kernel": "attention (one launch per step)"},
+            "pct_bf16_roofline": 100.0 * achieved / peak,
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": int(launches), "clocks": clocks.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def load_traffic():
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if one matching the current kernel exists; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            t = json.load(f)
+        return t.get(WORKLOAD)
+    except Exception:
+        return None
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

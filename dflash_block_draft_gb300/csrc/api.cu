@@ -1,0 +1,316 @@
+// api.cu -- the C ABI: host validation, workspace layout and kernel dispatch.
+//
+// Every entry point validates on the host before it launches anything, then
+// enqueues its kernels on the caller's stream and returns without
+// synchronising.  No device memory is allocated here.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dflash {
+
+// Per-device error word for conditions only a kernel can see.
+__device__ unsigned g_error_word;
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned*> g_err_ptr[kMaxDevices];
+
+unsigned* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned* p = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_error_word) != cudaSuccess) return nullptr;
+    p = static_cast<unsigned*>(addr);
+    g_err_ptr[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+bool env_flag(const char* name) {
+  const char* v = getenv(name);
+  return v && v[0] && strcmp(v, "0") != 0;
+}
+
+constexpr size_t kAlign = 256;
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t ctrl = 0;     // 256 B of counters for persistent kernels
+  size_t classes = 0;  // dense tile classes
+  size_t total = 0;
+};
+
+Layout layout_batched(int mode, int B, int S, int Q) {
+  Layout L;
+  L.ctrl = 0;
+  size_t off = kAlign;
+  if (mode == kDense) {
+    const size_t nqt = (size_t)(Q + kTileM - 1) / kTileM, nkt = (size_t)(S + Q + kTileN - 1) / kTileN;
+    L.classes = off;
+    off += round_up((size_t)B * nqt * nkt);
+  }
+  L.total = off;
+  return L;
+}
+
+Layout layout_ragged(int /*R*/) {
+  Layout L;
+  L.total = kAlign;
+  return L;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+dflash_status_t check_heads(int H, int dn, int dr, int dv) {
+  if (H <= 0 || dn < 0 || dr < 0 || dv <= 0 || dn + dr <= 0) return DFLASH_ERR_SHAPE;
+  if (dn + dr > DFLASH_MAX_DQK || dv > DFLASH_MAX_DV) return DFLASH_ERR_UNSUPPORTED;
+  return DFLASH_OK;
+}
+
+dflash_status_t check_dims(const dflash_dims_t* d) {
+  if (!d) return DFLASH_ERR_INVALID;
+  if (d->B < 0 || d->S < 0 || d->Q < 0) return DFLASH_ERR_SHAPE;
+  if (isnan(d->scale) || isinf(d->scale)) return DFLASH_ERR_INVALID;
+  const dflash_status_t st = check_heads(d->H, d->d_nope, d->d_rope, d->d_v);
+  if (st != DFLASH_OK) return st;
+  // Token and element counts must stay inside the kernels' index arithmetic.
+  const long long K = (long long)d->S + d->Q;
+  if (K >= (1ll << 31) - kTileN) return DFLASH_ERR_UNSUPPORTED;
+  if ((long long)d->B * K * d->H * (d->d_nope + d->d_rope + d->d_v) >= (1ll << 62)) return DFLASH_ERR_UNSUPPORTED;
+  if (d->B > 65535 || d->H > 65535) return DFLASH_ERR_UNSUPPORTED;
+  return DFLASH_OK;
+}
+
+dflash_status_t check_dtype(dflash_dtype_t t) {
+  return (t == DFLASH_BF16 || t == DFLASH_FP32) ? DFLASH_OK : DFLASH_ERR_DTYPE;
+}
+
+dflash_status_t check_tensors(const void* q, const void* kn, const void* kr, const void* v, void* out,
+                              const float* lse, int dr) {
+  if (!q || !kn || !v || !out || (dr > 0 && !kr)) return DFLASH_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(kn) || (dr > 0 && !aligned16(kr)) || !aligned16(v) || !aligned16(out))
+    return DFLASH_ERR_ALIGN;
+  if (lse && ((uintptr_t)lse & 3u)) return DFLASH_ERR_ALIGN;
+  return DFLASH_OK;
+}
+
+dflash_status_t check_workspace(const void* ws, size_t bytes, size_t need) {
+  if (bytes < need) return DFLASH_ERR_WORKSPACE;
+  if (need > 0 && (!ws || ((uintptr_t)ws % kAlign) != 0)) return DFLASH_ERR_WORKSPACE;
+  return DFLASH_OK;
+}
+
+float resolve_scale(float scale, int dn, int dr) {
+  return scale > 0.f ? scale : (float)(1.0 / sqrt((double)(dn + dr)));
+}
+
+AttnParams base_params(int H, int dn, int dr, int dv, float scale, const void* q, const void* kn,
+                       const void* kr, const void* v, void* out, float* lse) {
+  AttnParams p;
+  memset(&p, 0, sizeof p);
+  p.q = q;
+  p.kn = kn;
+  p.kr = kr;
+  p.v = v;
+  p.out = out;
+  p.lse = lse;
+  p.H = H;
+  p.dn = dn;
+  p.dr = dr;
+  p.dv = dv;
+  p.scale = resolve_scale(scale, dn, dr);
+  p.scale_log2 = (float)((double)p.scale * 1.4426950408889634);
+  p.err = error_word();
+  return p;
+}
+
+dflash_status_t launched(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA; }
+
+}  // namespace
+}  // namespace dflash
+
+using namespace dflash;
+
+extern "C" {
+
+const char* dflash_status_string(dflash_status_t s) {
+  switch (s) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID: return "invalid argument";
+    case DFLASH_ERR_SHAPE: return "inconsistent shapes";
+    case DFLASH_ERR_DTYPE: return "unsupported dtype";
+    case DFLASH_ERR_ALIGN: return "tensor not 16-byte aligned";
+    case DFLASH_ERR_UNSUPPORTED: return "shape beyond kernel limits";
+    case DFLASH_ERR_WORKSPACE: return "workspace null, misaligned or too small";
+    case DFLASH_ERR_CUDA: return "CUDA error";
+    case DFLASH_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t dflash_attn_workspace_size(int mode, const dflash_dims_t* dims, dflash_dtype_t dtype, int R, int H,
+                                  int d_nope, int d_rope, int d_v, int total_q, int total_kv,
+                                  int max_q_len) {
+  if (check_dtype(dtype) != DFLASH_OK) return 0;
+  if (mode == kDense || mode == kAnchored) {
+    if (check_dims(dims) != DFLASH_OK) return 0;
+    return layout_batched(mode, dims->B, dims->S, dims->Q).total;
+  }
+  if (mode == kRagged) {
+    if (R <= 0 || check_heads(H, d_nope, d_rope, d_v) != DFLASH_OK || total_q < 0 || total_kv < 0 ||
+        max_q_len < 0)
+      return 0;
+    return layout_ragged(R).total;
+  }
+  return 0;
+}
+
+dflash_status_t dflash_build_schedule_host(int B, int S, int Q, const int32_t* anchors, int nb, int block_size,
+                                           uint8_t* classes) {
+  if (B < 0 || S < 0 || Q < 0 || nb < 0 || block_size <= 0) return DFLASH_ERR_SHAPE;
+  if ((long long)nb * block_size != Q) return DFLASH_ERR_SHAPE;
+  if ((B > 0 && Q > 0 && !anchors) || !classes) return DFLASH_ERR_INVALID;
+  const int nqt = (Q + kTileM - 1) / kTileM, nkt = (S + Q + kTileN - 1) / kTileN;
+  for (long long i = 0; i < (long long)B * nb; ++i)
+    if (anchors[i] < 0 || anchors[i] > S) return DFLASH_ERR_INVALID;
+  for (int b = 0; b < B; ++b)
+    for (int qt = 0; qt < nqt; ++qt) {
+      const int r0 = qt * kTileM, r1 = r0 + kTileM < Q ? r0 + kTileM : Q;
+      int amin = S, amax = 0;
+      for (int j = r0 / block_size; j <= (r1 - 1) / block_size; ++j) {
+        const int a = anchors[(size_t)b * nb + j];
+        amin = a < amin ? a : amin;
+        amax = a > amax ? a : amax;
+      }
+      for (int kt = 0; kt < nkt; ++kt)
+        classes[((size_t)b * nqt + qt) * nkt + kt] =
+            (uint8_t)anchored_tile_class(S, Q, block_size, r0, r1, amin, amax, kt);
+    }
+  return DFLASH_OK;
+}
+
+dflash_status_t dflash_scan_mask(int B, int S, int Q, dflash_dtype_t dtype, const void* mask, uint8_t* classes,
+                                 dflash_stream_t stream) {
+  if (check_dtype(dtype) != DFLASH_OK) return DFLASH_ERR_DTYPE;
+  if (B < 0 || S < 0 || Q < 0) return DFLASH_ERR_SHAPE;
+  if (B == 0 || Q == 0) return DFLASH_OK;
+  if (!mask || !classes) return DFLASH_ERR_INVALID;
+  return launched(launch_mask_scan(mask, dtype == DFLASH_BF16, B, S, Q, classes, (cudaStream_t)stream));
+}
+
+dflash_status_t dflash_attn_dense(const dflash_dims_t* dims, dflash_dtype_t dtype, const void* q,
+                                  const void* k_nope, const void* k_rope, const void* v, const void* mask,
+                                  void* out, float* lse, void* workspace, size_t ws_bytes,
+                                  dflash_stream_t stream) {
+  dflash_status_t st;
+  if ((st = check_dtype(dtype)) != DFLASH_OK) return st;
+  if ((st = check_dims(dims)) != DFLASH_OK) return st;
+  if (dims->B == 0 || dims->Q == 0) return DFLASH_OK;
+  if ((st = check_tensors(q, k_nope, k_rope, v, out, lse, dims->d_rope)) != DFLASH_OK) return st;
+  if (!mask) return DFLASH_ERR_INVALID;
+  if (!aligned16(mask)) return DFLASH_ERR_ALIGN;
+  const Layout L = layout_batched(kDense, dims->B, dims->S, dims->Q);
+  if ((st = check_workspace(workspace, ws_bytes, L.total)) != DFLASH_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool bf16 = dtype == DFLASH_BF16;
+  uint8_t* classes = static_cast<uint8_t*>(workspace) + L.classes;
+  cudaError_t e = launch_mask_scan(mask, bf16, dims->B, dims->S, dims->Q, classes, s);
+  if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+  AttnParams p = base_params(dims->H, dims->d_nope, dims->d_rope, dims->d_v, dims->scale, q, k_nope, k_rope, v,
+                             out, lse);
+  p.mode = kDense;
+  p.mask = mask;
+  p.B = dims->B;
+  p.S = dims->S;
+  p.Q = dims->Q;
+  p.classes = classes;
+  p.nqt = (dims->Q + kTileM - 1) / kTileM;
+  p.nkt = (dims->S + dims->Q + kTileN - 1) / kTileN;
+  return launched(launch_attn_simt(p, bf16, dims->B, dims->Q, s));
+}
+
+dflash_status_t dflash_attn_anchored(const dflash_dims_t* dims, dflash_dtype_t dtype, const void* q,
+                                     const void* k_nope, const void* k_rope, const void* v,
+                                     const int32_t* anchors, int nb, int block_size, void* out, float* lse,
+                                     void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  dflash_status_t st;
+  if ((st = check_dtype(dtype)) != DFLASH_OK) return st;
+  if ((st = check_dims(dims)) != DFLASH_OK) return st;
+  if (block_size <= 0 || nb < 0 || (long long)nb * block_size != dims->Q) return DFLASH_ERR_SHAPE;
+  if (dims->B == 0 || dims->Q == 0) return DFLASH_OK;
+  if ((st = check_tensors(q, k_nope, k_rope, v, out, lse, dims->d_rope)) != DFLASH_OK) return st;
+  if (!anchors) return DFLASH_ERR_INVALID;
+  const Layout L = layout_batched(kAnchored, dims->B, dims->S, dims->Q);
+  if ((st = check_workspace(workspace, ws_bytes, L.total)) != DFLASH_OK) return st;
+  AttnParams p = base_params(dims->H, dims->d_nope, dims->d_rope, dims->d_v, dims->scale, q, k_nope, k_rope, v,
+                             out, lse);
+  p.mode = kAnchored;
+  p.B = dims->B;
+  p.S = dims->S;
+  p.Q = dims->Q;
+  p.nb = nb;
+  p.bs = block_size;
+  p.anchors = anchors;
+  return launched(launch_attn_simt(p, dtype == DFLASH_BF16, dims->B, dims->Q, (cudaStream_t)stream));
+}
+
+dflash_status_t dflash_attn_ragged(int R, int H, int d_nope, int d_rope, int d_v, float scale,
+                                   dflash_dtype_t dtype, const void* q, const void* k_nope, const void* k_rope,
+                                   const void* v, const int32_t* q_offsets, const int32_t* kv_offsets,
+                                   const int32_t* anchors, int block_size, int total_q, int total_kv,
+                                   int max_q_len, void* out, float* lse, void* workspace, size_t ws_bytes,
+                                   dflash_stream_t stream) {
+  dflash_status_t st;
+  if ((st = check_dtype(dtype)) != DFLASH_OK) return st;
+  if (R < 0 || total_q < 0 || total_kv < 0 || max_q_len < 0 || block_size <= 0) return DFLASH_ERR_SHAPE;
+  if ((st = check_heads(H, d_nope, d_rope, d_v)) != DFLASH_OK) return st;
+  if (isnan(scale) || isinf(scale)) return DFLASH_ERR_INVALID;
+  if (R > 65535 || H > 65535) return DFLASH_ERR_UNSUPPORTED;
+  if (R == 0 || total_q == 0) return DFLASH_OK;
+  if ((st = check_tensors(q, k_nope, k_rope, v, out, lse, d_rope)) != DFLASH_OK) return st;
+  if (!q_offsets || !kv_offsets || !anchors) return DFLASH_ERR_INVALID;
+  if (max_q_len == 0) return DFLASH_ERR_SHAPE;
+  const Layout L = layout_ragged(R);
+  if ((st = check_workspace(workspace, ws_bytes, L.total)) != DFLASH_OK) return st;
+  AttnParams p = base_params(H, d_nope, d_rope, d_v, scale, q, k_nope, k_rope, v, out, lse);
+  p.mode = kRagged;
+  p.R = R;
+  p.total_q = total_q;
+  p.total_kv = total_kv;
+  p.q_off = q_offsets;
+  p.kv_off = kv_offsets;
+  p.anchors = anchors;
+  p.bs = block_size;
+  return launched(launch_attn_simt(p, dtype == DFLASH_BF16, R, max_q_len, (cudaStream_t)stream));
+}
+
+uint64_t dflash_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+dflash_status_t dflash_last_device_error(dflash_stream_t stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DFLASH_ERR_CUDA;
+  unsigned* p = error_word();
+  if (!p) return DFLASH_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return DFLASH_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return DFLASH_ERR_CUDA;
+  }
+  return (dflash_status_t)v;
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dflash_attn.h"
+
+namespace dflash {
+
+struct AttnParams;
+
+// Tile class of key tile kt (keys [kt*TILE_N, min((kt+1)*TILE_N, S+Q))) for the
+// query rows [r0, r1) of one segment under the anchored rule, given the
+// minimum and maximum anchor of those rows (anchors clamped to [0, S]).
+//   context part [k0, min(k1,S)):  all rows see it iff min(k1,S) <= amin,
+//                                   no row sees it iff k0 >= amax;
+//   noise part: a row sees only its own block, so the rows together see the
+//   union of their blocks [blk(r0)*bs, min((blk(r1-1)+1)*bs, Q)), and every row
+//   sees every noise key only when all rows share one block that covers it.
+__host__ __device__ inline int anchored_tile_class(int S, int Q, int bs, int r0, int r1, int amin, int amax,
+                                                   int kt) {
+  const int K = S + Q;
+  const int k0 = kt * DFLASH_TILE_N;
+  const int k1 = k0 + DFLASH_TILE_N < K ? k0 + DFLASH_TILE_N : K;
+  const int c1 = k1 < S ? k1 : S;
+  bool ctx_all = true, ctx_none = true;
+  if (k0 < c1) {
+    ctx_all = c1 <= amin;
+    ctx_none = k0 >= amax;
+  }
+  const int n0 = (k0 > S ? k0 : S) - S, n1 = k1 - S;
+  bool nz_all = true, nz_none = true;
+  if (n0 < n1) {
+    const int b_lo = r0 / bs, b_hi = (r1 - 1) / bs;
+    const int u0 = b_lo * bs;
+    const int u1 = (b_hi + 1) * bs < Q ? (b_hi + 1) * bs : Q;
+    nz_none = n1 <= u0 || n0 >= u1;
+    nz_all = b_lo == b_hi && n0 >= u0 && n1 <= u1;
+  }
+  if (ctx_all && nz_all) return DFLASH_TILE_FULL;
+  if (ctx_none && nz_none) return DFLASH_TILE_SKIP;
+  return DFLASH_TILE_PARTIAL;
+}
+
+// Launch counter behind dflash_kernel_launches(); every launcher bumps it.
+void count_launch();
+
+size_t simt_smem_bytes(int dqk, int dv);
+cudaError_t launch_attn_simt(const AttnParams& p, bool bf16, int segments, int max_q, cudaStream_t stream);
+cudaError_t launch_mask_scan(const void* mask, bool bf16, int B, int S, int Q, uint8_t* classes,
+                             cudaStream_t stream);
+
+}  // namespace dflash

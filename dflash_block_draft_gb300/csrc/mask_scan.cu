@@ -1,0 +1,103 @@
+// mask_scan.cu -- classify every 128x128 tile of a dense additive mask.
+//
+// The dense entry point receives the DFlash block mask as an additive tensor
+// [B, 1, Q, S+Q] (KimiK3DFlashAttention.forward on the DFlash Kimi K3 draft
+// page passes it unchanged to SDPA).  Reading it once up front lets the
+// attention kernels skip all -inf tiles and skip mask reads on all-0 tiles.
+// The scan is bound by HBM: each mask byte is read exactly once, with 16-byte
+// loads when rows are 16-byte aligned.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dflash {
+namespace {
+
+constexpr int kScanThreads = 256;  // 2 threads per tile row, 64 keys each
+
+__device__ __forceinline__ void classify_bits(uint32_t bits, bool is_bf16, bool& zero, bool& neginf) {
+  if (is_bf16) {
+    zero = (bits & 0x7FFFu) == 0u;
+    neginf = bits == 0xFF80u;
+  } else {
+    zero = (bits & 0x7FFFFFFFu) == 0u;
+    neginf = bits == 0xFF800000u;
+  }
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kScanThreads) mask_scan_kernel(const void* __restrict__ mask, int S, int Q,
+                                                                 int nqt, int nkt, bool vec_ok,
+                                                                 uint8_t* __restrict__ classes) {
+  const int kt = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
+  const int K = S + Q;
+  const int row = qt * kTileM + (threadIdx.x >> 1);
+  const int c0 = kt * kTileN + (threadIdx.x & 1) * (kTileN / 2);
+  const int c1 = min(c0 + kTileN / 2, K);
+  bool all_zero = true, all_ninf = true;
+  if (row < Q && c0 < c1) {
+    const size_t base = ((size_t)b * Q + row) * (size_t)K;
+    if (vec_ok && c1 - c0 == kTileN / 2) {
+      // 64 keys = 128 B (bf16) or 256 B (fp32) as 16-byte vectors.
+      constexpr int kVec = kBf16 ? 8 : 16;
+      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const char*>(mask) +
+                                                      (base + c0) * (kBf16 ? 2 : 4));
+#pragma unroll
+      for (int t = 0; t < kVec; ++t) {
+        const uint4 w = __ldg(p + t);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          bool z0, n0;
+          if (kBf16) {
+            bool z1, n1;
+            classify_bits(ws[u] & 0xFFFFu, true, z0, n0);
+            classify_bits(ws[u] >> 16, true, z1, n1);
+            all_zero &= z0 && z1;
+            all_ninf &= n0 && n1;
+          } else {
+            classify_bits(ws[u], false, z0, n0);
+            all_zero &= z0;
+            all_ninf &= n0;
+          }
+        }
+      }
+    } else {
+      for (int c = c0; c < c1; ++c) {
+        uint32_t bits = kBf16 ? (uint32_t) static_cast<const uint16_t*>(mask)[base + c]
+                              : static_cast<const uint32_t*>(mask)[base + c];
+        bool z, n;
+        classify_bits(bits, kBf16, z, n);
+        all_zero &= z;
+        all_ninf &= n;
+      }
+    }
+  }
+  const int zero = __syncthreads_and(all_zero);
+  const int ninf = __syncthreads_and(all_ninf);
+  if (threadIdx.x == 0) {
+    uint8_t c = DFLASH_TILE_PARTIAL;
+    if (zero) c = DFLASH_TILE_FULL;
+    else if (ninf) c = DFLASH_TILE_SKIP;
+    classes[((size_t)b * nqt + qt) * nkt + kt] = c;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_mask_scan(const void* mask, bool bf16, int B, int S, int Q, uint8_t* classes,
+                             cudaStream_t stream) {
+  const int K = S + Q;
+  const int nqt = (Q + kTileM - 1) / kTileM, nkt = (K + kTileN - 1) / kTileN;
+  if (B == 0 || nqt == 0 || nkt == 0) return cudaSuccess;
+  const size_t esz = bf16 ? 2 : 4;
+  const bool vec_ok = ((uintptr_t)mask % 16 == 0) && ((size_t)K * esz) % 16 == 0;
+  const dim3 grid(nkt, nqt, B);
+  if (bf16)
+    mask_scan_kernel<true><<<grid, kScanThreads, 0, stream>>>(mask, S, Q, nqt, nkt, vec_ok, classes);
+  else
+    mask_scan_kernel<false><<<grid, kScanThreads, 0, stream>>>(mask, S, Q, nqt, nkt, vec_ok, classes);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -5,17 +5,23 @@ attention arithmetic and no visibility rule, so that both the CUDA library's
 tests and the fp64 oracle can take their inputs from it.
 
 Recipe (shared by every workload):
-  rng = numpy.random.default_rng(seed), seed = 1000 + workload index;
-  first the anchors (or, for the ragged workload, the context lengths), then
-  q, k_nope, k_rope, v drawn in that order as float32 standard normals, then
-  cast to bf16 with round-to-nearest-even for the bf16 workloads.
+  seed = 1000 + workload index;
+  anchors (or, for the ragged workload, the context lengths) come from
+  numpy.random.default_rng(seed);
+  q, k_nope, k_rope, v (tensor ids 0..3) are float32 standard normals drawn in
+  flat chunks of 2**22 elements, chunk c of tensor t from its own stream
+  Generator(PCG64(SeedSequence(seed, spawn_key=(t, c)))) so that chunks can be
+  drawn on several threads with a result that does not depend on the thread
+  count; bf16 workloads round them to bf16 (nearest, ties to even).
 Anchors are sorted, distinct and uniform without replacement over the stated
 range.  bf16 tensors are carried as uint16 bit patterns.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
+import os
 
 import numpy as np
 
@@ -93,9 +99,27 @@ def bf16_bits_to_f32(x: np.ndarray) -> np.ndarray:
     return (np.asarray(x, np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _normal(rng, shape, dtype):
-    a = rng.standard_normal(size=shape, dtype=np.float32)
-    return f32_to_bf16_bits(a) if dtype == "bf16" else a
+_CHUNK = 1 << 22
+
+
+def _normal(seed: int, tensor_id: int, shape, dtype: str) -> np.ndarray:
+    n = int(np.prod(shape))
+    out = np.empty(n, np.uint16 if dtype == "bf16" else np.float32)
+
+    def fill(c):
+        lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(tensor_id, c))))
+        a = g.standard_normal(size=hi - lo, dtype=np.float32)
+        out[lo:hi] = f32_to_bf16_bits(a) if dtype == "bf16" else a
+
+    nchunks = -(-n // _CHUNK)
+    if nchunks <= 1:
+        for c in range(nchunks):
+            fill(c)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=min(nchunks, os.cpu_count() or 4)) as ex:
+            list(ex.map(fill, range(nchunks)))
+    return out.reshape(shape)
 
 
 def sorted_distinct(rng, lo: int, hi: int, n: int) -> np.ndarray:
@@ -120,7 +144,8 @@ def make(w: Workload | str, seed: int | None = None, **override) -> dict:
         w = WORKLOADS[w]
     if override:
         w = dataclasses.replace(w, **override)
-    rng = np.random.default_rng(w.seed if seed is None else seed)
+    seed = w.seed if seed is None else seed
+    rng = np.random.default_rng(seed)
     dqk = w.d_nope + w.d_rope
     d = dict(workload=w, H=w.H, d_nope=w.d_nope, d_rope=w.d_rope, d_v=w.d_v,
              block_size=w.block_size, dtype=w.dtype)
@@ -135,16 +160,16 @@ def make(w: Workload | str, seed: int | None = None, **override) -> dict:
         anchors = np.repeat(ctx, w.nb).astype(np.int32)
         d.update(R=w.R, q_offsets=q_off.astype(np.int32), kv_offsets=kv_off.astype(np.int32),
                  anchors=anchors, context_lens=ctx.astype(np.int32), total_q=total_q, total_kv=total_kv,
-                 q=_normal(rng, (total_q, w.H, dqk), w.dtype),
-                 k_nope=_normal(rng, (total_kv, w.H, w.d_nope), w.dtype),
-                 k_rope=_normal(rng, (total_kv, w.d_rope), w.dtype),
-                 v=_normal(rng, (total_kv, w.H, w.d_v), w.dtype))
+                 q=_normal(seed, 0, (total_q, w.H, dqk), w.dtype),
+                 k_nope=_normal(seed, 1, (total_kv, w.H, w.d_nope), w.dtype),
+                 k_rope=_normal(seed, 2, (total_kv, w.d_rope), w.dtype),
+                 v=_normal(seed, 3, (total_kv, w.H, w.d_v), w.dtype))
         return d
     K = w.S + w.Q
     anchors = np.stack([sorted_distinct(rng, w.anchor_lo, w.anchor_hi, w.nb) for _ in range(w.B)])
     d.update(B=w.B, S=w.S, Q=w.Q, nb=w.nb, pad=w.pad, anchors=anchors,
-             q=_normal(rng, (w.B, w.Q, w.H, dqk), w.dtype),
-             k_nope=_normal(rng, (w.B, K, w.H, w.d_nope), w.dtype),
-             k_rope=_normal(rng, (w.B, K, w.d_rope), w.dtype),
-             v=_normal(rng, (w.B, K, w.H, w.d_v), w.dtype))
+             q=_normal(seed, 0, (w.B, w.Q, w.H, dqk), w.dtype),
+             k_nope=_normal(seed, 1, (w.B, K, w.H, w.d_nope), w.dtype),
+             k_rope=_normal(seed, 2, (w.B, K, w.d_rope), w.dtype),
+             v=_normal(seed, 3, (w.B, K, w.H, w.d_v), w.dtype))
     return d
