@@ -140,6 +140,15 @@ AttnParams base_params(int H, int dn, int dr, int dv, float scale, const void* q
 
 dflash_status_t launched(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA; }
 
+// The tensor-core kernel takes bf16 with the Kimi K3 MLA head dims and token
+// counts that fit TMA's 32-bit coordinates; DFLASH_FORCE_SIMT=1 routes every
+// call to the exact CUDA-core kernel instead (used to test both kernels).
+bool use_tc(dflash_dtype_t dtype, int dn, int dr, int dv, long long q_rows, long long kv_rows) {
+  if (dtype != DFLASH_BF16 || !tc_supported(dn, dr, dv)) return false;
+  if (q_rows + kTileM >= (1ll << 31) || kv_rows + kTileN >= (1ll << 31)) return false;
+  return !env_flag("DFLASH_FORCE_SIMT");
+}
+
 }  // namespace
 }  // namespace dflash
 
@@ -240,6 +249,9 @@ dflash_status_t dflash_attn_dense(const dflash_dims_t* dims, dflash_dtype_t dtyp
   p.classes = classes;
   p.nqt = (dims->Q + kTileM - 1) / kTileM;
   p.nkt = (dims->S + dims->Q + kTileN - 1) / kTileN;
+  const long long q_rows = (long long)dims->B * dims->Q, kv_rows = (long long)dims->B * (dims->S + dims->Q);
+  if (use_tc(dtype, dims->d_nope, dims->d_rope, dims->d_v, q_rows, kv_rows))
+    return launched(launch_attn_tc(p, dims->B, p.nqt, q_rows, kv_rows, s));
   return launched(launch_attn_simt(p, bf16, dims->B, dims->Q, s));
 }
 
@@ -265,6 +277,10 @@ dflash_status_t dflash_attn_anchored(const dflash_dims_t* dims, dflash_dtype_t d
   p.nb = nb;
   p.bs = block_size;
   p.anchors = anchors;
+  const long long q_rows = (long long)dims->B * dims->Q, kv_rows = (long long)dims->B * (dims->S + dims->Q);
+  if (use_tc(dtype, dims->d_nope, dims->d_rope, dims->d_v, q_rows, kv_rows))
+    return launched(launch_attn_tc(p, dims->B, (dims->Q + kTileM - 1) / kTileM, q_rows, kv_rows,
+                                   (cudaStream_t)stream));
   return launched(launch_attn_simt(p, dtype == DFLASH_BF16, dims->B, dims->Q, (cudaStream_t)stream));
 }
 
@@ -295,6 +311,9 @@ dflash_status_t dflash_attn_ragged(int R, int H, int d_nope, int d_rope, int d_v
   p.kv_off = kv_offsets;
   p.anchors = anchors;
   p.bs = block_size;
+  if (use_tc(dtype, d_nope, d_rope, d_v, total_q, total_kv))
+    return launched(launch_attn_tc(p, R, (max_q_len + kTileM - 1) / kTileM, total_q, total_kv,
+                                   (cudaStream_t)stream));
   return launched(launch_attn_simt(p, dtype == DFLASH_BF16, R, max_q_len, (cudaStream_t)stream));
 }
 

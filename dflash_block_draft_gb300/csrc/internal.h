@@ -49,6 +49,9 @@ void count_launch();
 
 size_t simt_smem_bytes(int dqk, int dv);
 cudaError_t launch_attn_simt(const AttnParams& p, bool bf16, int segments, int max_q, cudaStream_t stream);
+bool tc_supported(int dn, int dr, int dv);
+cudaError_t launch_attn_tc(const AttnParams& p, int segments, int nqt, long long q_rows, long long kv_rows,
+                           cudaStream_t stream);
 cudaError_t launch_mask_scan(const void* mask, bool bf16, int B, int S, int Q, uint8_t* classes,
                              cudaStream_t stream);
 

@@ -64,6 +64,8 @@ SMALL = [
     ("general_dims_fp32", "fp32", 2, 2, 200, 7, 12, 40, 24, 48),
     ("general_dims_bf16", "bf16", 1, 3, 150, 10, 4, 32, 16, 64),
     ("wide_blocks_fp32", "fp32", 1, 2, 90, 2, 150, 16, 8, 16),
+    # one block per row: the last key tile is FULL on its clipped extent and runs into the next row's keys
+    ("tc_one_block_straddle", "bf16", 3, 2, 300, 1, 16, 128, 64, 128),
 ]
 
 
@@ -72,9 +74,20 @@ def _small_case(dtype, B, H, S, nb, bs, dn, dr, dv, seed=123):
                       d_rope=dr, d_v=dv, anchor_lo=0, anchor_hi=S + 1)
 
 
+@pytest.fixture(params=["default", "simt"])
+def kernel(request, monkeypatch):
+    """Run a case on the default dispatch (tensor cores for the Kimi K3 MLA bf16
+    shape) and again with the exact CUDA-core kernel forced."""
+    if request.param == "simt":
+        monkeypatch.setenv("DFLASH_FORCE_SIMT", "1")
+    else:
+        monkeypatch.delenv("DFLASH_FORCE_SIMT", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
 @pytest.mark.parametrize("mode", ["anchored", "dense"])
-def test_small_cases_every_row(dfl, case, mode):
+def test_small_cases_every_row(dfl, case, mode, kernel):
     name, dtype, B, H, S, nb, bs, dn, dr, dv = case
     d = _small_case(dtype, B, H, S, nb, bs, dn, dr, dv)
     d["anchors"][0, 0] = 0  # own block only
@@ -109,7 +122,7 @@ def test_dense_general_mask_with_finite_values_and_empty_rows(dfl):
     assert np.all(got_o[1, 7] == 0) and np.all(np.isneginf(got_l[1, :, 7]))
 
 
-def test_single_visible_key_returns_value_row_exactly(dfl):
+def test_single_visible_key_returns_value_row_exactly(dfl, kernel):
     d = _small_case("bf16", 1, 2, 200, 20, 8, 128, 64, 128, seed=9)
     Q, K = d["Q"], d["S"] + d["Q"]
     mask = np.full((1, 1, Q, K), -np.inf, np.float32)
@@ -120,7 +133,7 @@ def test_single_visible_key_returns_value_row_exactly(dfl):
     np.testing.assert_array_equal(got_o[0], vals[0, pick])
 
 
-def test_dense_from_anchors_equals_anchored(dfl):
+def test_dense_from_anchors_equals_anchored(dfl, kernel):
     d = _small_case("bf16", 2, 2, 600, 30, 16, 128, 64, 128, seed=11)
     a_o, a_l = _run_batched(dfl, d, "anchored", "bf16")
     d_o, d_l = _run_batched(dfl, d, "dense", "bf16", _mask_for(d, "bf16"))
@@ -192,7 +205,7 @@ def _run_ragged(dfl, d, dtype, max_q_len=None):
 
 
 @pytest.mark.parametrize("dtype,dn,dr,dv", [("bf16", 128, 64, 128), ("fp32", 16, 8, 16)])
-def test_ragged_small_every_row(dfl, dtype, dn, dr, dv):
+def test_ragged_small_every_row(dfl, dtype, dn, dr, dv, kernel):
     d = synth.make("decode_bf16", seed=77, dtype=dtype, R=7, H=3, d_nope=dn, d_rope=dr, d_v=dv, ctx_lo=1,
                    ctx_hi=700, nb=3, block_size=8)
     # vary the anchors inside each request (they need not equal the context length)
@@ -205,6 +218,16 @@ def test_ragged_small_every_row(dfl, dtype, dn, dr, dv):
     got_o, got_l = _run_ragged(dfl, d, dtype)
     assert max_abs_err(got_o, want_o) <= TOL[dtype]
     assert max_abs_err(got_l, want_l) <= TOL[dtype]
+
+
+def test_ragged_decode_shape_small(dfl, kernel):
+    # decode shape (one block per request, anchor = context length) with short contexts
+    d = synth.make("decode_bf16", seed=80, R=9, H=3, ctx_lo=5, ctx_hi=700)
+    want_o, want_l = oracle.ragged(d["q"], d["k_nope"], d["k_rope"], d["v"], d["q_offsets"], d["kv_offsets"],
+                                   d["anchors"], d["block_size"])
+    got_o, got_l = _run_ragged(dfl, d, "bf16")
+    assert max_abs_err(got_o, want_o) <= TOL["bf16"]
+    assert max_abs_err(got_l, want_l) <= TOL["bf16"]
 
 
 def test_ragged_equals_per_request_anchored(dfl):
