@@ -6,20 +6,30 @@
 // KimiK3DFlashAttention, one K/V per query head; module docstring: the
 // qk_rope slice is a head-shared extension of the key, no rotary).
 //
-// One work item = (segment, 128-row query tile, head).  Per item the kernel
-// walks the 128-key tiles of [context | noise] that the schedule marks
-// FULL or PARTIAL (anchored rule, or the dense mask's tile classes) and keeps an
-// online softmax per row:
-//   S  = Q_nope K_nope^T + Q_rope K_rope^T      tcgen05 SS MMAs into TMEM (fp32)
-//   P  = exp2(S * scale * log2 e - m)           4 softmax warps, one row per thread
-//   O += P V                                    tcgen05 TS MMA, P (bf16) read from TMEM
+// One work item = (segment, pair of adjacent 128-row query tiles, head).  The
+// two query tiles ("halves" 0 and 1) share every K/V tile the item loads.  Per
+// item the kernel walks the 128-key tiles of [context | noise] that the
+// schedule marks FULL or PARTIAL for either half (anchored rule, or the dense
+// mask's tile classes) and keeps an online softmax per query row:
+//   S_i  = Q_i,nope K_nope^T + Q_i,rope K_rope^T    tcgen05 SS MMAs into TMEM (fp32)
+//   P_i  = exp2(S_i * scale * log2 e - m)           softmax warpgroup i, one row per thread
+//   O_i += P_i V                                    tcgen05 TS MMAs, P_i (bf16) read from TMEM
 //   out = O / l,  lse = (m + log2 l) ln 2
 //
-// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues MMAs, warps 2..5 run the softmax and the epilogue.  Shared memory holds
-// the Q tile (48 KB) and a 2-stage ring of K tiles (nope + rope, 48 KB) and V
-// tiles (32 KB), all in the 128-byte-swizzled K-major layout TMA writes.
-// TMEM (512 columns): S double buffer [0,256), O [256,384), P double buffer [384,512).
+// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues MMAs (warps 2, 3 idle), warps 4..7 and 8..11 are the softmax/epilogue
+// warpgroups of halves 0 and 1.  The first warpgroup gives registers back
+// (setmaxnreg 104) so that the softmax warpgroups get 200 registers a thread:
+// 128*104 + 256*200 = 384*168, the launch budget.  The MMA warp interleaves the halves,
+//   QK_0(j) QK_1(j) PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) PV_0(j+1) ...
+// so that one warpgroup's softmax overlaps the other half's MMAs.
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
+// P_i (bf16 pairs) overwrites the first 64 columns of S_i once they are read,
+// and QK_i(j+1) is issued only after PV_i(j), which the tensor pipe runs in order.
+// Shared memory: both Q tiles (96 KB) and a ring of eight 16 KB panels through
+// which the K tiles (nope 0-63, nope 64-127, rope: 3 panels) and V tiles
+// (v 0-63, v 64-127: 2 panels) stream in consumption order, all in the
+// 128-byte-swizzled layout TMA writes.
 // The grid is persistent (one CTA per SM); items are dealt in a snake order over
 // a longest-first list (query tiles with the most context first).
 // Every mbarrier wait is bounded; a wait that runs past its budget records
@@ -35,111 +45,138 @@ namespace {
 
 constexpr int kDn = 128, kDr = 64, kDv = 128;
 constexpr int kBM = 128, kBN = 128;
-constexpr uint32_t kPanel = kBM * 128;        // 128 rows x 128 bytes (64 bf16)
-constexpr uint32_t kQBytes = 3 * kPanel;      // nope 0-63, nope 64-127, rope
-constexpr uint32_t kKBytes = 3 * kPanel;
-constexpr uint32_t kVBytes = 2 * kPanel;      // v 0-63, v 64-127
-constexpr int kStages = 2;
+constexpr uint32_t kPanel = kBM * 128;    // 128 rows x 128 bytes (64 bf16)
+constexpr uint32_t kQBytes = 3 * kPanel;  // per half: nope 0-63, nope 64-127, rope
+constexpr uint32_t kRing = 8;             // ring panels
+constexpr uint32_t kPanelsPerTile = 5;    // K: 3, V: 2
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;
-constexpr uint32_t kOffV = kOffK + kStages * kKBytes;
-constexpr uint32_t kOffBar = kOffV + kStages * kVBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + alignment slack
+constexpr uint32_t kOffRing = 2 * kQBytes;
+constexpr uint32_t kOffBar = kOffRing + kRing * kPanel;
 
-// barrier slots (8 bytes each)
 enum {
   BAR_Q_FULL = 0,
   BAR_Q_EMPTY = 1,
-  BAR_K_FULL = 2,   // 2 stages
-  BAR_K_EMPTY = 4,  // 2
-  BAR_V_FULL = 6,   // 2
-  BAR_V_EMPTY = 8,  // 2 (also marks "PV of this tile done")
-  BAR_S_FULL = 10,  // 2
-  BAR_P_FULL = 12,  // 2
-  BAR_O_FULL = 14,
-  BAR_DRAIN = 15,
-  kNumBars = 16
+  BAR_RING_FULL = 2,                       // kRing
+  BAR_RING_EMPTY = BAR_RING_FULL + kRing,  // kRing
+  BAR_S_FULL = BAR_RING_EMPTY + kRing,     // 2 (per half)
+  BAR_P_FULL = BAR_S_FULL + 2,             // 2
+  BAR_O_FULL = BAR_P_FULL + 2,             // 2
+  BAR_DRAIN = BAR_O_FULL + 2,
+  kNumBars = BAR_DRAIN + 1
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + 8 * kNumBars;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr uint32_t kColS = 0, kColO = 256;  // S_i at kColS + 128 i, O_i at kColO + 128 i
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
+constexpr uint32_t kCtlRegs = 104, kSoftmaxRegs = 200;
+static_assert(128 * kCtlRegs + 256 * kSoftmaxRegs == kThreads * kLaunchRegs, "register split");
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s per wait
+constexpr uint32_t kSleepHintNs = 100000;           // re-check the budget every ~0.1 ms of sleep
 
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBM, kBN, 0, 0);  // Q, K both K-major
-constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, kDv, 0, 1);  // P from TMEM, V MN-major
+constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, 64, 0, 1);   // P from TMEM, V MN-major, 64 columns
 
 struct TcArgs {
   AttnParams p;
   int segments;
   int nqt;      // query tiles per segment (max over segments for ragged)
-  int n_items;  // nqt * segments * H
+  int npair;    // ceil(nqt / 2)
+  int n_items;  // npair * segments * H
   int mask_vec; // dense: mask rows are 16-byte aligned
 };
 
 struct Item {
   int ok;
-  int z, t, h;
+  int z, h;
   Seg sg;
-  int r0, r1;
-  int amin, amax;
+  int r0[2], r1[2];
+  int amin[2], amax[2];
+  bool has[2];
   int nkt;
-  const uint8_t* cls;
+  const uint8_t* cls[2];
+  int ctx_end, noise_begin, noise_end;  // anchored: the pair's non-SKIP tiles are [0,ctx_end) U [noise_begin,noise_end)
 };
 
 __device__ __forceinline__ Item decode_item(const TcArgs& a, int idx) {
   Item it;
   const AttnParams& p = a.p;
   const int zh = a.segments * p.H;
-  it.t = a.nqt - 1 - idx / zh;  // longest (latest) query tiles first
+  const int pair = a.npair - 1 - idx / zh;  // longest (latest) query tiles first
   const int rem = idx % zh;
   it.z = rem / p.H;
   it.h = rem % p.H;
   it.sg = resolve_segment(p, it.z);
   it.ok = it.sg.ok;
   if (!it.ok) return it;
-  it.r0 = it.t * kBM;
-  if (it.r0 >= it.sg.Q) {
-    it.ok = 0;
-    return it;
-  }
-  it.r1 = min(it.r0 + kBM, it.sg.Q);
-  it.nkt = (it.sg.S + it.sg.Q + kBN - 1) / kBN;
-  it.cls = nullptr;
-  it.amin = it.sg.S;
-  it.amax = 0;
-  if (p.mode == kDense) {
-    it.cls = p.classes + ((long long)it.z * p.nqt + it.t) * p.nkt;
-  } else {
-    for (int j = it.r0 / p.bs; j <= (it.r1 - 1) / p.bs; ++j) {
-      int an = p.anchors[it.sg.anc0 + j];
-      an = an < 0 ? 0 : (an > it.sg.S ? it.sg.S : an);
-      it.amin = min(it.amin, an);
-      it.amax = max(it.amax, an);
+  const int S = it.sg.S, Qn = it.sg.Q;
+  it.nkt = (S + Qn + kBN - 1) / kBN;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int t = 2 * pair + i;
+    it.r0[i] = t * kBM;
+    it.has[i] = it.r0[i] < Qn;
+    it.r1[i] = min(it.r0[i] + kBM, Qn);
+    it.cls[i] = nullptr;
+    it.amin[i] = S;
+    it.amax[i] = 0;
+    if (!it.has[i]) continue;
+    if (p.mode == kDense) {
+      it.cls[i] = p.classes + ((long long)it.z * p.nqt + t) * p.nkt;
+    } else {
+      for (int j = it.r0[i] / p.bs; j <= (it.r1[i] - 1) / p.bs; ++j) {
+        int an = p.anchors[it.sg.anc0 + j];
+        an = an < 0 ? 0 : (an > S ? S : an);
+        it.amin[i] = min(it.amin[i], an);
+        it.amax[i] = max(it.amax[i], an);
+      }
     }
+  }
+  it.ok = it.has[0];
+  if (it.ok && p.mode != kDense) {
+    // Context keys some row sees: k < max anchor.  Noise keys some row sees: the
+    // blocks of the pair's rows, [blk(first row) * bs, (blk(last row) + 1) * bs) within Q.
+    const int amax = max(it.amax[0], it.has[1] ? it.amax[1] : 0);
+    const int last = it.has[1] ? it.r1[1] : it.r1[0];
+    const int u0 = (it.r0[0] / p.bs) * p.bs;
+    const int u1 = min(((last - 1) / p.bs + 1) * p.bs, Qn);
+    it.ctx_end = (min(amax, S) + kBN - 1) / kBN;
+    it.noise_begin = (S + u0) / kBN;
+    it.noise_end = (S + u1 + kBN - 1) / kBN;
   }
   return it;
 }
 
-__device__ __forceinline__ int tile_class(const TcArgs& a, const Item& it, int kt) {
-  if (a.p.mode == kDense) return it.cls[kt];
-  return anchored_tile_class(it.sg.S, it.sg.Q, a.p.bs, it.r0, it.r1, it.amin, it.amax, kt);
-}
-
+// Next key tile after kt that either half needs (it.nkt when none is left).
 __device__ __forceinline__ int next_tile(const TcArgs& a, const Item& it, int kt) {
-  for (++kt; kt < it.nkt; ++kt)
-    if (tile_class(a, it, kt) != DFLASH_TILE_SKIP) return kt;
+  ++kt;
+  if (a.p.mode != kDense) {
+    if (kt < it.ctx_end) return kt;
+    kt = max(kt, it.noise_begin);
+    return kt < it.noise_end ? kt : it.nkt;
+  }
+  for (; kt < it.nkt; ++kt)
+    if (it.cls[0][kt] != DFLASH_TILE_SKIP || (it.has[1] && it.cls[1][kt] != DFLASH_TILE_SKIP)) return kt;
   return it.nkt;
 }
 
-// Item index of this CTA's round k (snake order), or -1 when past the end.
-__device__ __forceinline__ int item_of_round(const TcArgs& a, int k) {
+// Class of tile kt for the query tile of one half, from that half's scalars.
+__device__ __forceinline__ int half_class(const TcArgs& a, const Seg& sg, bool has, int r0, int r1, int amin,
+                                          int amax, const uint8_t* cls, int kt) {
+  if (!has) return DFLASH_TILE_SKIP;
+  if (a.p.mode == kDense) return cls[kt];
+  return anchored_tile_class(sg.S, sg.Q, a.p.bs, r0, r1, amin, amax, kt);
+}
+
+// Item index of this CTA's round k (snake order over the longest-first list).
+__device__ __forceinline__ int item_of_round(int k) {
   const int G = gridDim.x;
-  const int idx = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
-  return idx;
+  return k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
 }
 
 struct Ctl {
@@ -152,19 +189,99 @@ struct Ctl {
     const uint32_t b = bar(i);
     if (ptx::mbar_try_wait(b, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t n = 1;; ++n) {
-      if (ptx::mbar_try_wait(b, parity)) return true;
-      if ((n & 15u) == 0) {
-        if (*abort) return false;
-        if (ptx::globaltimer() - t0 > kWaitBudgetNs) {
-          *abort = 1;
-          record_error(err, DFLASH_ERR_TIMEOUT);
-          return false;
-        }
+    for (;;) {
+      // sleep on the barrier (woken by the phase completing) rather than spin
+      if (ptx::mbar_try_wait_sleep(b, parity, kSleepHintNs)) return true;
+      if (*abort) return false;
+      if (ptx::globaltimer() - t0 > kWaitBudgetNs) {
+        *abort = 1;
+        record_error(err, DFLASH_ERR_TIMEOUT);
+        return false;
       }
     }
   }
 };
+
+// How a softmax thread prepares a tile's scores for its row.
+enum { kPrepFull = 0, kPrepAnchored = 1, kPrepDense = 2, kPrepNone = 3 };
+
+struct PrepCtx {
+  int c_ctx, c_lo, c_hi;      // anchored: visible columns c < c_ctx or c_lo <= c < c_hi
+  const __nv_bfloat16* mask;  // dense: mask row at the tile's first key
+  int kmax;                   // dense: columns >= kmax lie past the segment
+  bool mvec;                  // dense: 16-byte mask loads allowed
+  float c2;                   // scale * log2(e)
+};
+
+__device__ __forceinline__ float max64(const float* x) {
+  float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 64; c += 8) {
+    a0 = ptx::max3(a0, x[c], x[c + 1]);
+    a1 = ptx::max3(a1, x[c + 2], x[c + 3]);
+    a2 = ptx::max3(a2, x[c + 4], x[c + 5]);
+    a3 = ptx::max3(a3, x[c + 6], x[c + 7]);
+  }
+  return ptx::max3(fmaxf(a0, a1), a2, a3);
+}
+
+__device__ __forceinline__ float dense_term(float s, float mk, float c2) {
+  // base-2 score with the additive mask; -inf stays -inf, huge finite values are
+  // clamped so that their base-2 image stays finite
+  return mk == -INFINITY ? -INFINITY : fmaf(s, c2, fmaxf(mk * kLog2e, -3.0e38f));
+}
+
+// Bits [lo, hi) of a 64-bit word, clipped to [0, 64).
+__device__ __forceinline__ uint64_t range_bits(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 64);
+  if (hi <= lo) return 0ull;
+  const uint64_t below_hi = hi >= 64 ? ~0ull : ((1ull << hi) - 1ull);
+  return below_hi & ~((1ull << lo) - 1ull);
+}
+
+// Applies the row's mask to the 64 scores of tile columns [c0, c0+64) in place:
+// FULL leaves raw scores, anchored sets hidden keys to -inf (raw scores stay
+// raw), dense turns scores into base-2 units plus the mask, NONE sets all -inf.
+__device__ __forceinline__ void mask64(float* x, int kind, int c0, const PrepCtx& pc) {
+  if (kind == kPrepFull) return;
+  if (kind == kPrepNone) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c) x[c] = -INFINITY;
+    return;
+  }
+  if (kind == kPrepAnchored) {
+    // visible: c < c_ctx (context below the anchor) or c_lo <= c < c_hi (own block)
+    const uint64_t vis = range_bits(0, pc.c_ctx - c0) | range_bits(pc.c_lo - c0, pc.c_hi - c0);
+    const uint32_t lo = (uint32_t)vis, hi = (uint32_t)(vis >> 32);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      x[c] = (lo >> c) & 1u ? x[c] : -INFINITY;
+      x[32 + c] = (hi >> c) & 1u ? x[32 + c] : -INFINITY;
+    }
+    return;
+  }
+  if (pc.mvec && pc.kmax >= c0 + 64) {
+    const uint4* mp = reinterpret_cast<const uint4*>(pc.mask + c0);
+#pragma unroll
+    for (int v8 = 0; v8 < 8; ++v8) {
+      const uint4 w = __ldg(mp + v8);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = v8 * 8 + u * 2;
+        x[c] = dense_term(x[c], __uint_as_float(ws[u] << 16), pc.c2);
+        x[c + 1] = dense_term(x[c + 1], __uint_as_float(ws[u] & 0xFFFF0000u), pc.c2);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      const float mk = c0 + c < pc.kmax ? __bfloat162float(pc.mask[c0 + c]) : -INFINITY;
+      x[c] = dense_term(x[c], mk, pc.c2);
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmQ,
@@ -185,15 +302,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(ctl.bar(BAR_Q_FULL), 1);
     ptx::mbar_init(ctl.bar(BAR_Q_EMPTY), 1);
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(ctl.bar(BAR_K_FULL + s), 1);
-      ptx::mbar_init(ctl.bar(BAR_K_EMPTY + s), 1);
-      ptx::mbar_init(ctl.bar(BAR_V_FULL + s), 1);
-      ptx::mbar_init(ctl.bar(BAR_V_EMPTY + s), 1);
-      ptx::mbar_init(ctl.bar(BAR_S_FULL + s), 1);
-      ptx::mbar_init(ctl.bar(BAR_P_FULL + s), 128);
+    for (uint32_t s = 0; s < kRing; ++s) {
+      ptx::mbar_init(ctl.bar(BAR_RING_FULL + s), 1);
+      ptx::mbar_init(ctl.bar(BAR_RING_EMPTY + s), 1);
     }
-    ptx::mbar_init(ctl.bar(BAR_O_FULL), 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ctl.bar(BAR_S_FULL + i), 1);
+      ptx::mbar_init(ctl.bar(BAR_P_FULL + i), 128);
+      ptx::mbar_init(ctl.bar(BAR_O_FULL + i), 1);
+    }
     ptx::mbar_init(ctl.bar(BAR_DRAIN), 1);
     *ctl.abort = 0;
     ptx::fence_mbar_init();
@@ -213,107 +330,151 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t ring = sbase + kOffRing;
+  if (warp < 4) ptx::setmaxnreg_dec<kCtlRegs>();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t g = 0, n_items = 0;
-      for (int k = 0;; ++k) {
-        const int idx = item_of_round(a, k);
-        if (k * (int)gridDim.x >= a.n_items) break;
+      uint32_t pc = 0, n_items = 0;  // ring panel counter, items loaded
+      bool stop = false;
+      for (int k = 0; !stop && k * (int)gridDim.x < a.n_items; ++k) {
+        const int idx = item_of_round(k);
         if (idx >= a.n_items) continue;
         const Item it = decode_item(a, idx);
         if (!it.ok) continue;
         if (n_items > 0 && !ctl.wait(BAR_Q_EMPTY, (n_items - 1) & 1u)) break;
-        const int qrow = (int)(it.sg.q0 + it.r0);
-        ptx::mbar_arrive_expect_tx(ctl.bar(BAR_Q_FULL), kQBytes);
-        for (int pn = 0; pn < 3; ++pn)
-          ptx::tma_load_3d(sbase + kOffQ + pn * kPanel, &tmQ, ctl.bar(BAR_Q_FULL), 64 * pn, it.h, qrow);
-        ++n_items;
-        bool stop = false;
-        for (int kt = next_tile(a, it, -1); kt < it.nkt; kt = next_tile(a, it, kt)) {
-          const int s = g & 1;
-          const uint32_t u = g >> 1;
-          const int krow = (int)(it.sg.kv0 + (long long)kt * kBN);
-          if (!ctl.wait(BAR_K_EMPTY + s, (u & 1u) ^ 1u)) { stop = true; break; }
-          const uint32_t kdst = sbase + kOffK + s * kKBytes;
-          ptx::mbar_arrive_expect_tx(ctl.bar(BAR_K_FULL + s), kKBytes);
-          ptx::tma_load_3d(kdst, &tmKn, ctl.bar(BAR_K_FULL + s), 0, it.h, krow);
-          ptx::tma_load_3d(kdst + kPanel, &tmKn, ctl.bar(BAR_K_FULL + s), 64, it.h, krow);
-          ptx::tma_load_2d(kdst + 2 * kPanel, &tmKr, ctl.bar(BAR_K_FULL + s), 0, krow);
-          if (!ctl.wait(BAR_V_EMPTY + s, (u & 1u) ^ 1u)) { stop = true; break; }
-          const uint32_t vdst = sbase + kOffV + s * kVBytes;
-          ptx::mbar_arrive_expect_tx(ctl.bar(BAR_V_FULL + s), kVBytes);
-          ptx::tma_load_3d(vdst, &tmV, ctl.bar(BAR_V_FULL + s), 0, it.h, krow);
-          ptx::tma_load_3d(vdst + kPanel, &tmV, ctl.bar(BAR_V_FULL + s), 64, it.h, krow);
-          ++g;
+        ptx::mbar_arrive_expect_tx(ctl.bar(BAR_Q_FULL), 2 * kQBytes);
+        for (int i = 0; i < 2; ++i) {
+          const int qrow = (int)(it.sg.q0 + it.r0[i]);
+          for (int pn = 0; pn < 3; ++pn)
+            ptx::tma_load_3d(sbase + kOffQ + i * kQBytes + pn * kPanel, &tmQ, ctl.bar(BAR_Q_FULL), 64 * pn, it.h,
+                             qrow);
         }
-        if (stop) break;
+        ++n_items;
+        for (int kt = next_tile(a, it, -1); kt < it.nkt && !stop; kt = next_tile(a, it, kt)) {
+          const int krow = (int)(it.sg.kv0 + (long long)kt * kBN);
+          for (uint32_t pn = 0; pn < kPanelsPerTile; ++pn, ++pc) {
+            const uint32_t s = pc % kRing;
+            if (!ctl.wait(BAR_RING_EMPTY + s, ((pc / kRing) & 1u) ^ 1u)) {
+              stop = true;
+              break;
+            }
+            const uint32_t dst = ring + s * kPanel;
+            const uint32_t fb = ctl.bar(BAR_RING_FULL + s);
+            ptx::mbar_arrive_expect_tx(fb, kPanel);
+            if (pn < 2) ptx::tma_load_3d(dst, &tmKn, fb, 64 * pn, it.h, krow);
+            else if (pn == 2) ptx::tma_load_2d(dst, &tmKr, fb, 0, krow);
+            else ptx::tma_load_3d(dst, &tmV, fb, 64 * (pn - 3), it.h, krow);
+          }
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t g = 0, n_items = 0;
-      const uint32_t sQ = sbase + kOffQ;
-      auto issue_qk = [&](uint32_t gg) -> bool {
-        const int s = gg & 1;
-        if (!ctl.wait(BAR_K_FULL + s, (gg >> 1) & 1u)) return false;
-        ptx::tc_fence_after();
-        const uint32_t sK = sbase + kOffK + s * kKBytes;
-        const uint32_t d = tmem + kColS + (uint32_t)s * kBN;
+      uint32_t g = 0, n_items = 0;  // global tile counter, items started
+      auto panel_ready = [&](uint32_t pcx) -> bool {
+        return ctl.wait(BAR_RING_FULL + pcx % kRing, (pcx / kRing) & 1u);
+      };
+      auto release = [&](uint32_t pcx) { ptx::tc_commit(ctl.bar(BAR_RING_EMPTY + pcx % kRing)); };
+      auto issue_qk = [&](int i, uint32_t gg) {
+        const uint32_t sQ = sbase + kOffQ + i * kQBytes;
+        const uint32_t d = tmem + kColS + 128u * i;
 #pragma unroll
         for (int ks = 0; ks < (kDn + kDr) / 16; ++ks) {
-          const uint32_t off = (uint32_t)(ks >> 2) * kPanel + (uint32_t)(ks & 3) * 32u;
-          ptx::mma_ss(d, ptx::smem_desc(sQ + off, 16, 1024), ptx::smem_desc(sK + off, 16, 1024), kIdescQK,
-                      ks > 0);
+          const uint32_t pn = (uint32_t)(ks >> 2);
+          const uint32_t kslot = (gg * kPanelsPerTile + pn) % kRing;
+          const uint32_t sub = (uint32_t)(ks & 3) * 32u;
+          ptx::mma_ss(d, ptx::smem_desc(sQ + pn * kPanel + sub, 16, 1024),
+                      ptx::smem_desc(ring + kslot * kPanel + sub, 16, 1024), kIdescQK, ks > 0);
         }
-        ptx::tc_commit(ctl.bar(BAR_S_FULL + s));
-        ptx::tc_commit(ctl.bar(BAR_K_EMPTY + s));
-        return true;
+        ptx::tc_commit(ctl.bar(BAR_S_FULL + i));
+      };
+      auto issue_pv = [&](int i, uint32_t gg, bool first) {
+        const uint32_t pcol = tmem + kColS + 128u * i;  // P_i aliases the head of S_i
+        const uint32_t d = tmem + kColO + 128u * i;
+#pragma unroll
+        for (uint32_t hv = 0; hv < 2; ++hv) {
+          const uint32_t vslot = (gg * kPanelsPerTile + 3u + hv) % kRing;
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            // 16 keys: 8 packed P columns; V rows: two 1024-byte groups of 8 keys
+            ptx::mma_ts(d + 64u * hv, pcol + (uint32_t)ks * 8u,
+                        ptx::smem_desc(ring + vslot * kPanel + (uint32_t)ks * 2048u, kPanel, 1024), kIdescPV,
+                        !(first && ks == 0));
+          }
+        }
       };
       bool stop = false;
-      for (int k = 0; !stop; ++k) {
-        const int idx = item_of_round(a, k);
-        if (k * (int)gridDim.x >= a.n_items) break;
+      for (int k = 0; !stop && k * (int)gridDim.x < a.n_items; ++k) {
+        const int idx = item_of_round(k);
         if (idx >= a.n_items) continue;
         const Item it = decode_item(a, idx);
         if (!it.ok) continue;
         if (!ctl.wait(BAR_Q_FULL, n_items & 1u)) break;
         ++n_items;
         int kt = next_tile(a, it, -1);
-        if (kt >= it.nkt) {  // nothing visible in this tile row: no MMA, release Q
+        if (kt >= it.nkt) {  // nothing visible for this pair of query tiles
           ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));
           continue;
         }
-        if (!issue_qk(g)) break;
-        for (int j = 0;; ++j) {
+        ptx::tc_fence_after();
+        bool first_tile = true, first_pv = true;
+        for (;;) {
           const int kn = next_tile(a, it, kt);
-          if (kn < it.nkt) {
-            if (!issue_qk(g + 1)) { stop = true; break; }
-          } else {
-            ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));
+          const uint32_t kp = g * kPanelsPerTile;  // first ring panel of tile g
+          if (!first_tile) {  // PV_0 of the previous tile
+            if (!ctl.wait(BAR_P_FULL + 0, (g - 1) & 1u) || !panel_ready(kp - 2) || !panel_ready(kp - 1)) {
+              stop = true;
+              break;
+            }
+            ptx::tc_fence_after();
+            issue_pv(0, g - 1, first_pv);
           }
-          const int s = g & 1;
-          const uint32_t par = (g >> 1) & 1u;
-          if (!ctl.wait(BAR_P_FULL + s, par) || !ctl.wait(BAR_V_FULL + s, par)) { stop = true; break; }
-          ptx::tc_fence_after();
-          const uint32_t sV = sbase + kOffV + s * kVBytes;
-          const uint32_t pcol = tmem + kColP + (uint32_t)s * 64u;
-#pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks) {
-            // P columns: 16 keys = 8 packed bf16x2 columns; V rows: 16 keys = 2 x 1024-byte groups.
-            ptx::mma_ts(tmem + kColO, pcol + (uint32_t)ks * 8u, ptx::smem_desc(sV + (uint32_t)ks * 2048u, kPanel, 1024),
-                        kIdescPV, (j > 0 || ks > 0));
-          }
-          ptx::tc_commit(ctl.bar(BAR_V_EMPTY + s));
-          ++g;
-          if (kn >= it.nkt) {
-            ptx::tc_commit(ctl.bar(BAR_O_FULL));
+          if (!panel_ready(kp) || !panel_ready(kp + 1) || !panel_ready(kp + 2)) {
+            stop = true;
             break;
           }
+          ptx::tc_fence_after();
+          issue_qk(0, g);
+          if (!first_tile) {  // PV_1 of the previous tile; its V panels are then free
+            if (!ctl.wait(BAR_P_FULL + 1, (g - 1) & 1u)) {
+              stop = true;
+              break;
+            }
+            ptx::tc_fence_after();
+            issue_pv(1, g - 1, first_pv);
+            first_pv = false;
+            release(kp - 2);
+            release(kp - 1);
+          }
+          issue_qk(1, g);
+          release(kp);
+          release(kp + 1);
+          release(kp + 2);
+          first_tile = false;
+          ++g;
+          if (kn >= it.nkt) break;
           kt = kn;
         }
+        if (stop) break;
+        ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));  // every QK of this item has been issued
+        // PV of the item's last tile for both halves
+        const uint32_t kp = g * kPanelsPerTile;
+        if (!panel_ready(kp - 2) || !panel_ready(kp - 1)) break;
+        for (int i = 0; i < 2; ++i) {
+          if (!ctl.wait(BAR_P_FULL + i, (g - 1) & 1u)) {
+            stop = true;
+            break;
+          }
+          ptx::tc_fence_after();
+          issue_pv(i, g - 1, first_pv);
+          ptx::tc_commit(ctl.bar(BAR_O_FULL + i));
+        }
+        if (stop) break;
+        release(kp - 2);
+        release(kp - 1);
       }
       // Drain: every MMA this thread issued has finished before TMEM is released.
       ptx::tc_commit(ctl.bar(BAR_DRAIN));
@@ -325,22 +486,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue (warps 2..5)
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue (warps 4..11)
+    ptx::setmaxnreg_inc<kSoftmaxRegs>();
+    const int half = (warp - 4) >> 2;  // query tile of the pair
     const int quad = warp & 3;
-    const int row = quad * 32 + lane;             // TMEM lane = query row within the tile
+    const int row = quad * 32 + lane;  // TMEM lane = query row within the tile
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_col = tmem + lane_off + kColS + 128u * half;
+    const uint32_t o_col = tmem + lane_off + kColO + 128u * half;
     const float c2 = p.scale_log2;
     uint32_t g = 0, n_full = 0;
     bool stop = false;
-    for (int k = 0; !stop; ++k) {
-      const int idx = item_of_round(a, k);
-      if (k * (int)gridDim.x >= a.n_items) break;
+    for (int k = 0; !stop && k * (int)gridDim.x < a.n_items; ++k) {
+      const int idx = item_of_round(k);
       if (idx >= a.n_items) continue;
       const Item it = decode_item(a, idx);
       if (!it.ok) continue;
-      const int i = it.r0 + row;
-      const bool row_ok = i < it.r1;
+      // this half's scalars (selected, so that the item's arrays stay in registers)
+      const bool h_has = half ? it.has[1] : it.has[0];
+      const int h_r0 = half ? it.r0[1] : it.r0[0], h_r1 = half ? it.r1[1] : it.r1[0];
+      const int h_amin = half ? it.amin[1] : it.amin[0], h_amax = half ? it.amax[1] : it.amax[0];
+      const uint8_t* h_cls = half ? it.cls[1] : it.cls[0];
+      const int i = h_r0 + row;
+      const bool row_ok = h_has && i < h_r1;
       const int S = it.sg.S, Qn = it.sg.Q, K = S + Qn;
       int ctx_lim = 0, nlo = 0, nhi = 0;
       const __nv_bfloat16* mrow = nullptr;
@@ -356,116 +525,85 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool any_tile = false;
       for (int kt = next_tile(a, it, -1); kt < it.nkt; kt = next_tile(a, it, kt)) {
         any_tile = true;
-        const int cls = tile_class(a, it, kt);
-        const int s = g & 1;
-        if (!ctl.wait(BAR_S_FULL + s, (g >> 1) & 1u)) { stop = true; break; }
-        ptx::tc_fence_after();
-        float x[kBN];
-        {
-          uint32_t* xr = reinterpret_cast<uint32_t*>(x);
-          const uint32_t sa = tmem + lane_off + kColS + (uint32_t)s * kBN;
-          ptx::tmem_ld32(sa, xr);
-          ptx::tmem_ld32(sa + 32, xr + 32);
-          ptx::tmem_ld32(sa + 64, xr + 64);
-          ptx::tmem_ld32(sa + 96, xr + 96);
-          ptx::tmem_wait_ld();
-        }
+        const int cls = half_class(a, it.sg, h_has, h_r0, h_r1, h_amin, h_amax, h_cls, kt);
         const int k0 = kt * kBN;
-        float mt = -INFINITY;
-        bool scaled = false;  // x already in base-2 units (dense partial tiles)
-        // A FULL tile that runs past the segment's last key still needs the
+        // How this row treats the tile: plain scores, anchored mask, dense mask, or
+        // nothing.  A FULL tile that runs past the segment's last key still needs the
         // per-key test: the columns past S+Q hold the next segment's keys.
-        const bool full = cls == DFLASH_TILE_FULL && k0 + kBN <= K;
-        if (!row_ok) {
-#pragma unroll
-          for (int c = 0; c < kBN; ++c) x[c] = -INFINITY;
-        } else if (full) {
-#pragma unroll
-          for (int c = 0; c < kBN; ++c) mt = fmaxf(mt, x[c]);
-        } else if (p.mode != kDense) {
-          // anchored: context keys k < ctx_lim, noise keys of the row's own block
-          const int c_ctx = ctx_lim - k0, c_lo = nlo - k0, c_hi = nhi - k0;
-#pragma unroll
-          for (int c = 0; c < kBN; ++c) {
-            const bool vis = c < c_ctx || (c >= c_lo && c < c_hi);
-            x[c] = vis ? x[c] : -INFINITY;
-            mt = fmaxf(mt, x[c]);
-          }
-        } else {
-          scaled = true;
-          const int kmax = K - k0;
-          if (a.mask_vec && kmax >= kBN) {
-            const uint4* mp = reinterpret_cast<const uint4*>(mrow + k0);
-#pragma unroll
-            for (int v8 = 0; v8 < kBN / 8; ++v8) {
-              const uint4 w = __ldg(mp + v8);
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                  const int c = v8 * 8 + u * 2 + hh;
-                  const float mk = __uint_as_float((hh ? (ws[u] & 0xFFFF0000u) : (ws[u] << 16)));
-                  x[c] = mk == -INFINITY ? -INFINITY : fmaf(x[c], c2, fmaxf(mk * kLog2e, -3.0e38f));
-                  mt = fmaxf(mt, x[c]);
-                }
-              }
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-              const float mk = c < kmax ? __bfloat162float(mrow[k0 + c]) : -INFINITY;
-              x[c] = mk == -INFINITY ? -INFINITY : fmaf(x[c], c2, fmaxf(mk * kLog2e, -3.0e38f));
-              mt = fmaxf(mt, x[c]);
-            }
-          }
+        int kind;
+        if (!row_ok || cls == DFLASH_TILE_SKIP) kind = kPrepNone;
+        else if (cls == DFLASH_TILE_FULL && k0 + kBN <= K) kind = kPrepFull;
+        else kind = p.mode == kDense ? kPrepDense : kPrepAnchored;
+        const PrepCtx pc{ctx_lim - k0, nlo - k0, nhi - k0, mrow ? mrow + k0 : nullptr, K - k0,
+                         a.mask_vec != 0, c2};
+        if (!ctl.wait(BAR_S_FULL + half, g & 1u)) {
+          stop = true;
+          break;
         }
-        const float m_tile = scaled ? mt : mt * c2;  // base-2 units
+        ptx::tc_fence_after();
+        // pass 1: row maximum over the tile, 64 columns at a time (the scores are
+        // read again in pass 2 rather than held in registers)
+        float mt = -INFINITY;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float x[64];
+          ptx::tmem_ld32(s_col + 64u * hh, reinterpret_cast<uint32_t*>(x));
+          ptx::tmem_ld32(s_col + 64u * hh + 32u, reinterpret_cast<uint32_t*>(x) + 32);
+          ptx::tmem_wait_ld();
+          mask64(x, kind, 64 * hh, pc);
+          mt = fmaxf(mt, max64(x));
+        }
+        const bool scaled = kind == kPrepDense;  // dense scores are already in base-2 units
+        const float m_tile = scaled ? mt : mt * c2;
         if (m_tile != -INFINITY) {
           if (m_used == -INFINITY) {
             m_used = m_tile;  // nothing accumulated for this row yet
           } else if (m_tile > m_used + 8.0f) {
-            // Rescale O and l to the new maximum once PV of the previous tile is done.
+            // Rescale O and l to the new maximum.  PV of the previous tile was
+            // issued before this tile's QK, so S_FULL already covers its completion.
             const float alpha = ptx::ex2(m_used - m_tile);
-            const uint32_t gp = g - 1;
-            if (!ctl.wait(BAR_V_EMPTY + (gp & 1), (gp >> 1) & 1u)) { stop = true; break; }
-            ptx::tc_fence_after();
-            const uint32_t oa = tmem + lane_off + kColO;
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < kDv; cc += 32) {
               uint32_t o[32];
-              ptx::tmem_ld32(oa + cc, o);
+              ptx::tmem_ld32(o_col + cc, o);
               ptx::tmem_wait_ld();
 #pragma unroll
               for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              ptx::tmem_st32(oa + cc, o);
+              ptx::tmem_st32(o_col + cc, o);
             }
             ptx::tmem_wait_st();
             l *= alpha;
             m_used = m_tile;
           }
         }
+        // pass 2: p = exp2(x - m), packed to bf16 pairs (lower key in the low half),
+        // written over the first 64 columns of S; columns 0-63 are re-read before
+        // P overwrites 0-31, and P's 32-63 land on columns already consumed.
         const float msub = m_used == -INFINITY ? 0.f : m_used;
-        // p = exp2(x - m) packed to bf16 pairs (lower key in the low half), written to TMEM in two halves.
-        const float mul = scaled ? 1.f : c2;
-        float lsum = 0.f;
-        const uint32_t pa = tmem + lane_off + kColP + (uint32_t)s * 64u;
+        const float2 mul2 = make_float2(scaled ? 1.f : c2, scaled ? 1.f : c2);
+        const float2 neg2 = make_float2(-msub, -msub);
+        float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int hh = 0; hh < 2; ++hh) {
+          float x[64];
+          ptx::tmem_ld32(s_col + 64u * hh, reinterpret_cast<uint32_t*>(x));
+          ptx::tmem_ld32(s_col + 64u * hh + 32u, reinterpret_cast<uint32_t*>(x) + 32);
+          ptx::tmem_wait_ld();
+          mask64(x, kind, 64 * hh, pc);
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
-            const float p0 = ptx::ex2(fmaf(x[64 * half + c], mul, -msub));
-            const float p1 = ptx::ex2(fmaf(x[64 * half + c + 1], mul, -msub));
-            lsum += p0 + p1;
-            pk[c / 2] = ptx::pack_bf16x2(p0, p1);
+            const float2 arg = __ffma2_rn(make_float2(x[c], x[c + 1]), mul2, neg2);
+            const float2 pp = make_float2(ptx::ex2(arg.x), ptx::ex2(arg.y));
+            lsum = __fadd2_rn(lsum, pp);
+            pk[c / 2] = ptx::pack_bf16x2(pp.x, pp.y);
           }
-          ptx::tmem_st32(pa + 32u * half, pk);
+          ptx::tmem_st32(s_col + 32u * hh, pk);
         }
-        l += lsum;
+        l += lsum.x + lsum.y;
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(ctl.bar(BAR_P_FULL + s));
+        ptx::mbar_arrive(ctl.bar(BAR_P_FULL + half));
         ++g;
       }
       if (stop) break;
@@ -473,14 +611,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ob[kDv / 2];
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (any_tile) {
-        if (!ctl.wait(BAR_O_FULL, n_full & 1u)) break;
+        if (!ctl.wait(BAR_O_FULL + half, n_full & 1u)) break;
         ++n_full;
         ptx::tc_fence_after();
-        const uint32_t oa = tmem + lane_off + kColO;
 #pragma unroll
         for (int cc = 0; cc < kDv; cc += 32) {
           uint32_t o[32];
-          ptx::tmem_ld32(oa + cc, o);
+          ptx::tmem_ld32(o_col + cc, o);
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
@@ -570,7 +707,8 @@ cudaError_t launch_attn_tc(const AttnParams& p, int segments, int nqt, long long
   a.p = p;
   a.segments = segments;
   a.nqt = nqt;
-  a.n_items = nqt * segments * p.H;
+  a.npair = (nqt + 1) / 2;
+  a.n_items = a.npair * segments * p.H;
   a.mask_vec = 0;
   if (p.mode == kDense) a.mask_vec = (((uintptr_t)p.mask & 15u) == 0) && ((p.S + p.Q) % 8 == 0);
   if (a.n_items <= 0) return cudaSuccess;
@@ -580,6 +718,11 @@ cudaError_t launch_attn_tc(const AttnParams& p, int segments, int nqt, long long
     return cudaErrorInvalidValue;
   const int nsm = sm_count();
   if (nsm <= 0) return cudaErrorInvalidDevice;
+  // The setmaxnreg split assumes the kernel launches with exactly kLaunchRegs
+  // registers per thread; any other count would make setmaxnreg.inc wait forever.
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, attn_tc_kernel) != cudaSuccess || fa.numRegs != kLaunchRegs)
+    return cudaErrorInvalidConfiguration;
   const int grid = a.n_items < nsm ? a.n_items : nsm;
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
