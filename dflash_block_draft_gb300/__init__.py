@@ -33,7 +33,7 @@ STATUS = {0: "DFLASH_OK", 1: "DFLASH_ERR_INVALID", 2: "DFLASH_ERR_SHAPE", 3: "DF
 
 EXPORTS = ("dflash_attn_dense", "dflash_attn_anchored", "dflash_attn_ragged", "dflash_attn_workspace_size",
            "dflash_build_schedule_host", "dflash_scan_mask", "dflash_status_string", "dflash_last_device_error",
-           "dflash_kernel_launches")
+           "dflash_kernel_launches", "dflash_attn_dense_noalloc")
 
 
 class DFlashError(RuntimeError):
@@ -75,6 +75,8 @@ def load_library(path: str | None = None):
         lib.dflash_status_string.argtypes = [I]
         lib.dflash_status_string.restype = ctypes.c_char_p
         lib.dflash_last_device_error.argtypes = [P]
+        lib.dflash_attn_dense_noalloc.argtypes = [DP, I, P, P, P, P, P, P, P, P]
+        lib.dflash_attn_dense_noalloc.restype = ctypes.c_int
         lib.dflash_kernel_launches.argtypes = []
         lib.dflash_kernel_launches.restype = ctypes.c_uint64
         for name in ("dflash_attn_dense", "dflash_attn_anchored", "dflash_attn_ragged",
@@ -190,6 +192,28 @@ def dflash_attn_dense(q, k_nope, k_rope, v, mask, out=None, lse=None, scale=0.0,
                                _dev_ptr(lse, "lse", torch.float32), _dev_ptr(ws, "workspace"), nbytes,
                                _stream(stream))
     _check("dflash_attn_dense", st)
+    return out
+
+
+def dflash_attn_dense_noalloc(q, k_nope, k_rope, v, mask, out=None, lse=None, scale=0.0, stream=None):
+    """dflash_attn_dense without a workspace: the library's own fixed device
+    array holds the mask-tile classes (see include/dflash_attn.h).  For callers
+    that cannot allocate device scratch memory; concurrent calls on one device
+    must not overlap on the GPU."""
+    torch = _torch()
+    lib = load_library()
+    B, H, S, Q, dn, dr, dv = _batched_shapes(q, k_nope, k_rope, v)
+    dt = _dtype_code(q)
+    if tuple(mask.shape) != (B, 1, Q, S + Q):
+        raise ValueError("mask must be [B,1,Q,S+Q]")
+    if out is None:
+        out = torch.empty((B, Q, H, dv), dtype=q.dtype, device=q.device)
+    d = _dims(B, H, S, Q, dn, dr, dv, scale)
+    st = lib.dflash_attn_dense_noalloc(ctypes.byref(d), dt, _dev_ptr(q, "q"), _dev_ptr(k_nope, "k_nope", q.dtype),
+                                       _dev_ptr(k_rope, "k_rope", q.dtype), _dev_ptr(v, "v", q.dtype),
+                                       _dev_ptr(mask, "mask", q.dtype), _dev_ptr(out, "out", q.dtype),
+                                       _dev_ptr(lse, "lse", torch.float32), _stream(stream))
+    _check("dflash_attn_dense_noalloc", st)
     return out
 
 

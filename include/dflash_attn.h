@@ -158,6 +158,34 @@ DFLASH_API dflash_status_t dflash_attn_ragged(int R, int H, int d_nope, int d_ro
                                    void* out, float* lse, void* workspace, size_t ws_bytes,
                                    dflash_stream_t stream);
 
+/*
+ * Dense entry point that allocates nothing and takes no workspace.  (No
+ * counterpart on the pages: this is a convenience of this library.)
+ *
+ * For callers that cannot provide device scratch memory -- runtimes that plan
+ * all device memory once at start-up and forbid allocations while serving,
+ * or plugin interfaces whose fixed signature has no workspace argument.  The
+ * dense path's only scratch, one class byte per 128x128 mask tile, lives in a
+ * fixed device array inside the library (DFLASH_NOALLOC_MAX_TILES + 256 bytes,
+ * held on every GPU that loads the library until the process exits).
+ * Arguments and results are those of dflash_attn_dense.
+ *   - Returns DFLASH_ERR_WORKSPACE when B * ceil(Q/128) * ceil((S+Q)/128)
+ *     exceeds DFLASH_NOALLOC_MAX_TILES; nothing is launched then.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array, which keeps the previous call's
+ *     contents (each call rewrites every byte it reads).  Calls that overlap
+ *     on the GPU (different streams, or different host threads on one device)
+ *     race on it and must be serialised by the caller.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define DFLASH_NOALLOC_MAX_TILES (1 << 20)
+DFLASH_API dflash_status_t dflash_attn_dense_noalloc(const dflash_dims_t* dims, dflash_dtype_t dtype,
+                                                     const void* q, const void* k_nope, const void* k_rope,
+                                                     const void* v, const void* mask, void* out, float* lse,
+                                                     dflash_stream_t stream);
+
 enum { DFLASH_MODE_DENSE = 0, DFLASH_MODE_ANCHORED = 1, DFLASH_MODE_RAGGED = 2 };
 
 /*
