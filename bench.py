@@ -362,6 +362,70 @@ def run_ours(args):
     return 0
 
 
+def run_decode(args):
+    """The ragged decode workload: 64 requests x 16 draft rows, contexts
+    log-uniform in [1024, 32768], H=32.  HBM-bound: the roofline is bytes."""
+    import torch
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    import dflash_block_draft_gb300 as dfl
+    dfl.load_library()
+    d = synth.make("decode_bf16")
+    H, bs = d["H"], d["block_size"]
+    work = metrics.ragged_work(d["q_offsets"], d["kv_offsets"], d["anchors"], H, bs, d["d_nope"], d["d_rope"],
+                               d["d_v"])
+    dev = {k: to_dev(d[k], "bf16", device) for k in ("q", "k_nope", "k_rope", "v")}
+    qo, ko, an = (torch.from_numpy(d[k]).to(device) for k in ("q_offsets", "kv_offsets", "anchors"))
+    out = torch.empty((d["total_q"], H, d["d_v"]), dtype=torch.bfloat16, device=device)
+    nbytes = dfl.dflash_attn_workspace_size(dfl.MODE_RAGGED, H=H, d_nope=d["d_nope"], d_rope=d["d_rope"],
+                                            d_v=d["d_v"], R=d["R"], total_q=d["total_q"], total_kv=d["total_kv"],
+                                            max_q_len=16)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def step():
+        dfl.dflash_attn_ragged(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], qo, ko, an, bs, 16, out=out,
+                               workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    if dfl.dflash_last_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(0)
+    launches0 = dfl.dflash_kernel_launches()
+    torch.cuda.synchronize(device)
+    clocks.start()
+    for k in range(args.steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(device)
+    clocks.stop()
+    launches = dfl.dflash_kernel_launches() - launches0
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    peaks, src = load_peaks()
+    gbs = work["bytes"] / (ms / 1e3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    line = {"metric": "DFlash block-attn ragged decode: algorithmic HBM GB/s (and unmasked TFLOP/s)",
+            "value": gbs, "unit": "GB/s", "tflops": work["flops"] / (ms / 1e3) / 1e12, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"decode_bf16: R={d['R']} x 16 rows, H={H}, contexts log-uniform [1024,32768], "
+                                   f"total_kv={d['total_kv']}", "l2": "flushed between timed steps (256 MiB write)",
+                       "algorithmic_bytes_per_step": work["bytes"], "unmasked_flops_per_step": work["flops"]},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": None, "peak_source": f"hbm_gbs ({src})",
+                         "kernel": "plan + split attention + combine (one step)"},
+            "gpu_launches": int(launches), "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def load_traffic():
     """DRAM bytes per launch of the attention kernel from the committed ncu
     summary, when it was taken on the kernel source as it is now; else None."""
@@ -390,11 +454,15 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["prefill_bf16", "decode_bf16"], default="prefill_bf16",
+                    help="prefill_bf16 (the headline) or the ragged decode workload (HBM-bound)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "decode_bf16":
+        return run_decode(args)
     return run_ours(args)
 
 

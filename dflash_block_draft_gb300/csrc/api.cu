@@ -67,10 +67,17 @@ Layout layout_batched(int mode, int B, int S, int Q) {
   return L;
 }
 
-Layout layout_ragged(int /*R*/) {
+Layout layout_ragged(int R, int H, bool decode, int total_kv) {
   Layout L;
-  L.total = kAlign;
+  L.total = kAlign + (decode ? round_up(decode_workspace_bytes(R, H, total_kv)) : 0);
   return L;
+}
+
+// Ragged batches whose requests have at most 16 rows take the split-context
+// decode kernels (bf16, Kimi K3 MLA head dims).
+bool use_decode(dflash_dtype_t dtype, int dn, int dr, int dv, int max_q_len) {
+  return dtype == DFLASH_BF16 && decode_supported(dn, dr, dv, max_q_len) && !env_flag("DFLASH_FORCE_SIMT") &&
+         !env_flag("DFLASH_NO_SPLIT");
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -183,7 +190,7 @@ size_t dflash_attn_workspace_size(int mode, const dflash_dims_t* dims, dflash_dt
     if (R <= 0 || check_heads(H, d_nope, d_rope, d_v) != DFLASH_OK || total_q < 0 || total_kv < 0 ||
         max_q_len < 0)
       return 0;
-    return layout_ragged(R).total;
+    return layout_ragged(R, H, use_decode(dtype, d_nope, d_rope, d_v, max_q_len), total_kv).total;
   }
   return 0;
 }
@@ -300,7 +307,8 @@ dflash_status_t dflash_attn_ragged(int R, int H, int d_nope, int d_rope, int d_v
   if ((st = check_tensors(q, k_nope, k_rope, v, out, lse, d_rope)) != DFLASH_OK) return st;
   if (!q_offsets || !kv_offsets || !anchors) return DFLASH_ERR_INVALID;
   if (max_q_len == 0) return DFLASH_ERR_SHAPE;
-  const Layout L = layout_ragged(R);
+  const bool decode = use_decode(dtype, d_nope, d_rope, d_v, max_q_len);
+  const Layout L = layout_ragged(R, H, decode, total_kv);
   if ((st = check_workspace(workspace, ws_bytes, L.total)) != DFLASH_OK) return st;
   AttnParams p = base_params(H, d_nope, d_rope, d_v, scale, q, k_nope, k_rope, v, out, lse);
   p.mode = kRagged;
@@ -311,6 +319,8 @@ dflash_status_t dflash_attn_ragged(int R, int H, int d_nope, int d_rope, int d_v
   p.kv_off = kv_offsets;
   p.anchors = anchors;
   p.bs = block_size;
+  if (decode && (long long)total_q + kTileM < (1ll << 31) && (long long)total_kv + kTileN < (1ll << 31))
+    return launched(launch_attn_decode(p, static_cast<uint8_t*>(workspace) + kAlign, (cudaStream_t)stream));
   if (use_tc(dtype, d_nope, d_rope, d_v, total_q, total_kv))
     return launched(launch_attn_tc(p, R, (max_q_len + kTileM - 1) / kTileM, total_q, total_kv,
                                    (cudaStream_t)stream));

@@ -648,11 +648,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
+}  // namespace
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn() {
+static EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     void* f = nullptr;
@@ -665,25 +667,24 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// rows x heads x width (bf16), box = 64 x 1 x 128, 128-byte swizzle.
-bool make_map_3d(CUtensorMap* m, const void* base, long long rows, int heads, int width) {
+bool make_map_3d(CUtensorMap* m, const void* base, long long rows, int heads, int width, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)heads, (cuuint64_t)rows};
   const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * heads};
-  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   const cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_map_2d(CUtensorMap* m, const void* base, long long rows, int width) {
+bool make_map_2d(CUtensorMap* m, const void* base, long long rows, int width, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)width * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -696,8 +697,6 @@ int sm_count() {
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   return n;
 }
-
-}  // namespace
 
 bool tc_supported(int dn, int dr, int dv) { return dn == kDn && dr == kDr && dv == kDv; }
 
@@ -713,8 +712,8 @@ cudaError_t launch_attn_tc(const AttnParams& p, int segments, int nqt, long long
   if (p.mode == kDense) a.mask_vec = (((uintptr_t)p.mask & 15u) == 0) && ((p.S + p.Q) % 8 == 0);
   if (a.n_items <= 0) return cudaSuccess;
   CUtensorMap mq, mkn, mkr, mv;
-  if (!make_map_3d(&mq, p.q, q_rows, p.H, kDn + kDr) || !make_map_3d(&mkn, p.kn, kv_rows, p.H, kDn) ||
-      !make_map_2d(&mkr, p.kr, kv_rows, kDr) || !make_map_3d(&mv, p.v, kv_rows, p.H, kDv))
+  if (!make_map_3d(&mq, p.q, q_rows, p.H, kDn + kDr, kBM) || !make_map_3d(&mkn, p.kn, kv_rows, p.H, kDn, kBN) ||
+      !make_map_2d(&mkr, p.kr, kv_rows, kDr, kBN) || !make_map_3d(&mv, p.v, kv_rows, p.H, kDv, kBN))
     return cudaErrorInvalidValue;
   const int nsm = sm_count();
   if (nsm <= 0) return cudaErrorInvalidDevice;

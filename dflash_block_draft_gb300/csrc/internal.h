@@ -1,6 +1,7 @@
 // internal.h -- declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -49,9 +50,20 @@ void count_launch();
 
 size_t simt_smem_bytes(int dqk, int dv);
 cudaError_t launch_attn_simt(const AttnParams& p, bool bf16, int segments, int max_q, cudaStream_t stream);
+// TMA tensor maps over bf16 tensors, 128-byte swizzle, box {64, 1, box_rows} / {64, box_rows}.
+bool make_map_3d(CUtensorMap* m, const void* base, long long rows, int heads, int width, int box_rows);
+bool make_map_2d(CUtensorMap* m, const void* base, long long rows, int width, int box_rows);
+int sm_count();
+
 bool tc_supported(int dn, int dr, int dv);
 cudaError_t launch_attn_tc(const AttnParams& p, int segments, int nqt, long long q_rows, long long kv_rows,
                            cudaStream_t stream);
+// Split-context decode path (ragged batches with at most 16 rows per request).
+bool decode_supported(int dn, int dr, int dv, int max_q_len);
+int decode_max_units(int R, int total_kv);
+size_t decode_workspace_bytes(int R, int H, int total_kv);
+cudaError_t launch_attn_decode(const AttnParams& p, void* ws, cudaStream_t stream);
+
 cudaError_t launch_mask_scan(const void* mask, bool bf16, int B, int S, int Q, uint8_t* classes,
                              cudaStream_t stream);
 

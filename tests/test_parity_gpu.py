@@ -230,6 +230,32 @@ def test_ragged_decode_shape_small(dfl, kernel):
     assert max_abs_err(got_l, want_l) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("bs,nb,seed", [(16, 1, 81), (8, 2, 82), (4, 4, 83)])
+def test_ragged_decode_split_context_every_row(dfl, bs, nb, seed):
+    # 16 draft rows per request (split-context kernels), contexts that cross the
+    # 2048-key split boundaries, anchors anywhere in [0, S_r]
+    d = synth.make("decode_bf16", seed=seed, R=6, H=2, ctx_lo=1500, ctx_hi=9000, nb=nb, block_size=bs)
+    rng = np.random.default_rng(seed)
+    for r in range(6):
+        S_r = int(d["kv_offsets"][r + 1] - d["kv_offsets"][r]) - 16
+        d["anchors"][nb * r:nb * r + nb] = np.sort(rng.integers(0, S_r + 1, size=nb))
+    d["anchors"][0] = 0
+    want_o, want_l = oracle.ragged(d["q"], d["k_nope"], d["k_rope"], d["v"], d["q_offsets"], d["kv_offsets"],
+                                   d["anchors"], bs)
+    got_o, got_l = _run_ragged(dfl, d, "bf16")
+    assert max_abs_err(got_o, want_o) <= TOL["bf16"]
+    assert max_abs_err(got_l, want_l) <= TOL["bf16"]
+
+
+def test_ragged_split_equals_unsplit(dfl, monkeypatch):
+    d = synth.make("decode_bf16", seed=84, R=5, H=2, ctx_lo=100, ctx_hi=6000)
+    split_o, split_l = _run_ragged(dfl, d, "bf16")
+    monkeypatch.setenv("DFLASH_NO_SPLIT", "1")  # one pass over each request's whole context
+    full_o, full_l = _run_ragged(dfl, d, "bf16")
+    assert max_abs_err(split_o, full_o) <= TOL["bf16"]
+    assert max_abs_err(split_l, full_l) <= 1e-3
+
+
 def test_ragged_equals_per_request_anchored(dfl):
     d = synth.make("decode_bf16", seed=78, R=4, H=2, ctx_lo=100, ctx_hi=900, nb=2, block_size=16)
     got_o, _ = _run_ragged(dfl, d, "bf16")
