@@ -46,16 +46,17 @@ constexpr uint32_t kPanelsPerTile = 5;      // k_nope x2, k_rope, v x2
 constexpr uint32_t kOffRing = 0;
 constexpr uint32_t kOffQ = kOffRing + kRing * kPanel;
 constexpr uint32_t kOffP = kOffQ + 3 * kQPanel;
-constexpr uint32_t kOffBar = kOffP + 2 * kQPanel;
+constexpr uint32_t kOffBar = kOffP + 4 * kQPanel;  // P^T double buffer, 2 panels each
 
 enum {
   BAR_Q_FULL = 0,
   BAR_Q_EMPTY = 1,
   BAR_RING_FULL = 2,
   BAR_RING_EMPTY = BAR_RING_FULL + kRing,
-  BAR_S_FULL = BAR_RING_EMPTY + kRing,
-  BAR_P_FULL = BAR_S_FULL + 1,
-  BAR_O_FULL = BAR_P_FULL + 1,
+  BAR_S_FULL = BAR_RING_EMPTY + kRing,  // 2: S^T double buffer
+  BAR_P_FULL = BAR_S_FULL + 2,          // 2: P^T double buffer
+  BAR_PV_DONE = BAR_P_FULL + 2,         // one phase per PV
+  BAR_O_FULL = BAR_PV_DONE + 1,
   BAR_DRAIN = BAR_O_FULL + 1,
   kNumBars = BAR_DRAIN + 1
 };
@@ -67,7 +68,7 @@ constexpr uint32_t kSmemBytes = kOffRed + 4 * kRedFloats + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmemCols = 64;
-constexpr uint32_t kColS = 0, kColO = 32;
+constexpr uint32_t kColS = 0, kColO = 32;  // S^T buffers at 0 and 16
 
 constexpr int kThreads = 192;
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;
@@ -183,8 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ctl.bar(BAR_RING_FULL + s), 1);
       ptx::mbar_init(ctl.bar(BAR_RING_EMPTY + s), 1);
     }
-    ptx::mbar_init(ctl.bar(BAR_S_FULL), 1);
-    ptx::mbar_init(ctl.bar(BAR_P_FULL), 128);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ctl.bar(BAR_S_FULL + b), 1);
+      ptx::mbar_init(ctl.bar(BAR_P_FULL + b), 128);
+    }
+    ptx::mbar_init(ctl.bar(BAR_PV_DONE), 1);
     ptx::mbar_init(ctl.bar(BAR_O_FULL), 1);
     ptx::mbar_init(ctl.bar(BAR_DRAIN), 1);
     *ctl.abort = 0;
@@ -251,45 +255,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!it.ok) continue;
         if (!ctl.wait(BAR_Q_FULL, n & 1u)) break;
         ++n;
-        bool first = true;
-        int kt = next_tile(a, it, it.kt0 - 1);
-        for (; kt < it.kt1; kt = next_tile(a, it, kt), ++g) {
-          const uint32_t kp = g * kPanelsPerTile;
-          bool ok = true;
-          for (uint32_t pn = 0; pn < 3 && ok; ++pn)
-            ok = ctl.wait(BAR_RING_FULL + (kp + pn) % kRing, ((kp + pn) / kRing) & 1u);
-          if (!ok) { stop = true; break; }
+        // S^T of the next tile is computed while the softmax works on this one.
+        auto issue_qk = [&](uint32_t gg) -> bool {
+          const uint32_t kp = gg * kPanelsPerTile;
+          for (uint32_t pn = 0; pn < 3; ++pn)
+            if (!ctl.wait(BAR_RING_FULL + (kp + pn) % kRing, ((kp + pn) / kRing) & 1u)) return false;
           ptx::tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < (kDn + kDr) / 16; ++ks) {
             const uint32_t pn = (uint32_t)(ks >> 2), sub = (uint32_t)(ks & 3) * 32u;
             const uint32_t kslot = (kp + pn) % kRing;
-            ptx::mma_ss(tmem + kColS, ptx::smem_desc(ring + kslot * kPanel + sub, 16, 1024),
+            ptx::mma_ss(tmem + kColS + 16u * (gg & 1u), ptx::smem_desc(ring + kslot * kPanel + sub, 16, 1024),
                         ptx::smem_desc(sQ + pn * kQPanel + sub, 16, 1024), kIdescQK, ks > 0);
           }
-          ptx::tc_commit(ctl.bar(BAR_S_FULL));
+          ptx::tc_commit(ctl.bar(BAR_S_FULL + (gg & 1u)));
           for (uint32_t pn = 0; pn < 3; ++pn) ptx::tc_commit(ctl.bar(BAR_RING_EMPTY + (kp + pn) % kRing));
-          // P^T of this tile, then O^T += V^T P^T
-          if (!ctl.wait(BAR_P_FULL, g & 1u) || !ctl.wait(BAR_RING_FULL + (kp + 3) % kRing, ((kp + 3) / kRing) & 1u) ||
+          return true;
+        };
+        int kt = next_tile(a, it, it.kt0 - 1);
+        if (kt >= it.kt1) {  // nothing visible in this split
+          ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));
+          continue;
+        }
+        if (!issue_qk(g)) break;
+        bool first = true;
+        for (;;) {
+          const int kn = next_tile(a, it, kt);
+          if (kn < it.kt1) {
+            if (!issue_qk(g + 1)) { stop = true; break; }
+          } else {
+            ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));
+          }
+          // O^T += V^T P^T for tile g
+          const uint32_t kp = g * kPanelsPerTile;
+          if (!ctl.wait(BAR_P_FULL + (g & 1u), (g >> 1) & 1u) ||
+              !ctl.wait(BAR_RING_FULL + (kp + 3) % kRing, ((kp + 3) / kRing) & 1u) ||
               !ctl.wait(BAR_RING_FULL + (kp + 4) % kRing, ((kp + 4) / kRing) & 1u)) {
             stop = true;
             break;
           }
           ptx::tc_fence_after();
           const uint32_t v0 = ring + ((kp + 3) % kRing) * kPanel;  // the two V panels are adjacent
+          const uint32_t sPg = sP + (g & 1u) * 2u * kQPanel;
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks) {
             ptx::mma_ss(tmem + kColO, ptx::smem_desc(v0 + (uint32_t)ks * 2048u, kPanel, 1024),
-                        ptx::smem_desc(sP + (uint32_t)(ks >> 2) * kQPanel + (uint32_t)(ks & 3) * 32u, 16, 1024),
+                        ptx::smem_desc(sPg + (uint32_t)(ks >> 2) * kQPanel + (uint32_t)(ks & 3) * 32u, 16, 1024),
                         kIdescPV, !(first && ks == 0));
           }
           first = false;
+          ptx::tc_commit(ctl.bar(BAR_PV_DONE));
           ptx::tc_commit(ctl.bar(BAR_RING_EMPTY + (kp + 3) % kRing));
           ptx::tc_commit(ctl.bar(BAR_RING_EMPTY + (kp + 4) % kRing));
+          ++g;
+          if (kn >= it.kt1) break;
+          kt = kn;
         }
         if (stop) break;
-        ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));
-        if (!first) ptx::tc_commit(ctl.bar(BAR_O_FULL));  // only units that ran a PV
+        ptx::tc_commit(ctl.bar(BAR_O_FULL));
       }
       ptx::tc_commit(ctl.bar(BAR_DRAIN));
       const uint64_t t0 = ptx::globaltimer();
@@ -326,13 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kt = next_tile(a, it, it.kt0 - 1); kt < it.kt1; kt = next_tile(a, it, kt), ++g) {
         const int key = kt * kBN + t;  // this thread's key, relative to the request
         const bool full = unit_class(a, it, kt) == DFLASH_TILE_FULL && kt * kBN + kBN <= K;
-        if (!ctl.wait(BAR_S_FULL, g & 1u)) {
+        if (!ctl.wait(BAR_S_FULL + (g & 1u), (g >> 1) & 1u)) {
           stop = true;
           break;
         }
         ptx::tc_fence_after();
         float x[kQN];
-        ptx::tmem_ld16(tmem + lane_off + kColS, reinterpret_cast<uint32_t*>(x));
+        ptx::tmem_ld16(tmem + lane_off + kColS + 16u * (g & 1u), reinterpret_cast<uint32_t*>(x));
         ptx::tmem_wait_ld();
         uint32_t flags = 0;
 #pragma unroll
@@ -380,8 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             rescale = true;
           }
           if (rescale && !first) {
-            // O^T column q (this thread's dv lane) scaled to the new reference; PV of
-            // the previous tile has completed (it was issued before this tile's QK).
+            // O^T column q (this thread's dv lane) scaled to the new reference, once
+            // PV of the previous tile has completed.
+            if (!ctl.wait(BAR_PV_DONE, (g - 1) & 1u)) {
+              stop = true;
+              break;
+            }
+            ptx::tc_fence_after();
             uint32_t o[kQN];
             ptx::tmem_ld16(tmem + lane_off + kColO, o);
             ptx::tmem_wait_ld();
@@ -393,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::named_barrier(kSoftmaxBarrier, 128);  // red[] is free again
         }
         // p = exp2(x - m_ref); P^T[row q][key t] in the 128-byte-swizzled K-major layout
-        uint8_t* pt = smem + kOffP + (t >> 6) * kQPanel;
+        uint8_t* pt = smem + kOffP + (g & 1u) * 2u * kQPanel + (t >> 6) * kQPanel;
         const int cb = (t & 63) * 2;  // byte offset of this key inside a 128-byte row
 #pragma unroll
         for (int q = 0; q < kQN; ++q) {
@@ -404,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::fence_proxy_async_smem();  // P^T written by threads, read by the tensor core
         ptx::tc_fence_before();
-        ptx::mbar_arrive(ctl.bar(BAR_P_FULL));
+        ptx::mbar_arrive(ctl.bar(BAR_P_FULL + (g & 1u)));
         first = false;
       }
       if (stop) break;
