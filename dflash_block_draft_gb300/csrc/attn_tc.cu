@@ -19,8 +19,8 @@
 // Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
 // issues MMAs (warps 2, 3 idle), warps 4..7 and 8..11 are the softmax/epilogue
 // warpgroups of halves 0 and 1.  The first warpgroup gives registers back
-// (setmaxnreg 104) so that the softmax warpgroups get 200 registers a thread:
-// 128*104 + 256*200 = 384*168, the launch budget.  The MMA warp interleaves the halves,
+// (setmaxnreg 120) so that the softmax warpgroups get 192 registers a thread:
+// 128*120 + 256*192 = 384*168, the launch budget.  The MMA warp interleaves the halves,
 //   QK_0(j) QK_1(j) PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) PV_0(j+1) ...
 // so that one warpgroup's softmax overlaps the other half's MMAs.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
@@ -74,7 +74,7 @@ constexpr uint32_t kColS = 0, kColO = 256;  // S_i at kColS + 128 i, O_i at kCol
 
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
-constexpr uint32_t kCtlRegs = 104, kSoftmaxRegs = 200;
+constexpr uint32_t kCtlRegs = 120, kSoftmaxRegs = 192;
 static_assert(128 * kCtlRegs + 256 * kSoftmaxRegs == kThreads * kLaunchRegs, "register split");
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s per wait
 constexpr uint32_t kSleepHintNs = 100000;           // re-check the budget every ~0.1 ms of sleep
@@ -378,30 +378,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         return ctl.wait(BAR_RING_FULL + pcx % kRing, (pcx / kRing) & 1u);
       };
       auto release = [&](uint32_t pcx) { ptx::tc_commit(ctl.bar(BAR_RING_EMPTY + pcx % kRing)); };
+      // Descriptors are built once; a k-step only adds its byte offset >> 4 to the
+      // start-address field (every operand lies below 256 KB, so the 14-bit field
+      // never carries).
+      const uint64_t dQ0 = ptx::smem_desc(sbase + kOffQ, 16, 1024);
+      const uint64_t dRingK = ptx::smem_desc(ring, 16, 1024);
+      const uint64_t dRingV = ptx::smem_desc(ring, kPanel, 1024);
       auto issue_qk = [&](int i, uint32_t gg) {
-        const uint32_t sQ = sbase + kOffQ + i * kQBytes;
+        const uint32_t s0 = (gg * kPanelsPerTile) % kRing;
+        const uint64_t dq = dQ0 + ((i * kQBytes) >> 4);
         const uint32_t d = tmem + kColS + 128u * i;
 #pragma unroll
         for (int ks = 0; ks < (kDn + kDr) / 16; ++ks) {
-          const uint32_t pn = (uint32_t)(ks >> 2);
-          const uint32_t kslot = (gg * kPanelsPerTile + pn) % kRing;
-          const uint32_t sub = (uint32_t)(ks & 3) * 32u;
-          ptx::mma_ss(d, ptx::smem_desc(sQ + pn * kPanel + sub, 16, 1024),
-                      ptx::smem_desc(ring + kslot * kPanel + sub, 16, 1024), kIdescQK, ks > 0);
+          const uint32_t pn = (uint32_t)(ks >> 2), sub = (uint32_t)(ks & 3) * 32u;
+          const uint32_t kslot = (s0 + pn) % kRing;
+          ptx::mma_ss(d, dq + ((pn * kPanel + sub) >> 4), dRingK + ((kslot * kPanel + sub) >> 4), kIdescQK, ks > 0);
         }
         ptx::tc_commit(ctl.bar(BAR_S_FULL + i));
       };
       auto issue_pv = [&](int i, uint32_t gg, bool first) {
+        const uint32_t s0 = (gg * kPanelsPerTile) % kRing;
         const uint32_t pcol = tmem + kColS + 128u * i;  // P_i aliases the head of S_i
         const uint32_t d = tmem + kColO + 128u * i;
 #pragma unroll
         for (uint32_t hv = 0; hv < 2; ++hv) {
-          const uint32_t vslot = (gg * kPanelsPerTile + 3u + hv) % kRing;
+          const uint64_t dv = dRingV + ((((s0 + 3u + hv) % kRing) * kPanel) >> 4);
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks) {
             // 16 keys: 8 packed P columns; V rows: two 1024-byte groups of 8 keys
-            ptx::mma_ts(d + 64u * hv, pcol + (uint32_t)ks * 8u,
-                        ptx::smem_desc(ring + vslot * kPanel + (uint32_t)ks * 2048u, kPanel, 1024), kIdescPV,
+            ptx::mma_ts(d + 64u * hv, pcol + (uint32_t)ks * 8u, dv + (((uint32_t)ks * 2048u) >> 4), kIdescPV,
                         !(first && ks == 0));
           }
         }
