@@ -16,13 +16,14 @@
 //   O_i += P_i V                                    tcgen05 TS MMAs, P_i (bf16) read from TMEM
 //   out = O / l,  lse = (m + log2 l) ln 2
 //
-// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues MMAs (warps 2, 3 idle), warps 4..7 and 8..11 are the softmax/epilogue
-// warpgroups of halves 0 and 1.  The first warpgroup gives registers back
-// (setmaxnreg 120) so that the softmax warpgroups get 192 registers a thread:
-// 128*120 + 256*192 = 384*168, the launch budget.  The MMA warp interleaves the halves,
-//   QK_0(j) QK_1(j) PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) PV_0(j+1) ...
-// so that one warpgroup's softmax overlaps the other half's MMAs.
+// Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM, warps 1
+// and 2 issue the MMAs of halves 0 and 1 (warp 3 idle), warps 4..7 and 8..11
+// are the softmax/epilogue warpgroups of halves 0 and 1.  The first warpgroup
+// gives registers back (setmaxnreg 120) so that the softmax warpgroups get 192
+// registers a thread: 128*120 + 256*192 = 384*168, the launch budget.  Each
+// half's MMAs go out from its own thread in the order
+//   QK_i(j) [softmax_i(j)] PV_i(j) QK_i(j+1) ...
+// so the tensor pipe runs one half's MMAs while the other half's softmax works.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
 // P_i (bf16 pairs) overwrites the first 64 columns of S_i once they are read,
 // and QK_i(j+1) is issued only after PV_i(j), which the tensor pipe runs in order.
@@ -301,17 +302,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ctl.bar(BAR_Q_FULL), 1);
-    ptx::mbar_init(ctl.bar(BAR_Q_EMPTY), 1);
+    ptx::mbar_init(ctl.bar(BAR_Q_EMPTY), 2);  // both MMA issuers
     for (uint32_t s = 0; s < kRing; ++s) {
       ptx::mbar_init(ctl.bar(BAR_RING_FULL + s), 1);
-      ptx::mbar_init(ctl.bar(BAR_RING_EMPTY + s), 1);
+      ptx::mbar_init(ctl.bar(BAR_RING_EMPTY + s), 2);  // both MMA issuers
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ctl.bar(BAR_S_FULL + i), 1);
       ptx::mbar_init(ctl.bar(BAR_P_FULL + i), 128);
       ptx::mbar_init(ctl.bar(BAR_O_FULL + i), 1);
     }
-    ptx::mbar_init(ctl.bar(BAR_DRAIN), 1);
+    ptx::mbar_init(ctl.bar(BAR_DRAIN), 2);  // both MMA issuers
     *ctl.abort = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -370,9 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues the MMAs of half 0, warp 2 those of half 1, each in its own
+    // order  PV_i(j-1) QK_i(j) PV_i(j) QK_i(j+1) ...  so that a late softmax of one
+    // half never holds back the other half's MMAs.  Ring panels and the Q buffer
+    // are released when both halves have committed (their barriers count 2).
     if (lane == 0) {
+      const int i = warp - 1;
       uint32_t g = 0, n_items = 0;  // global tile counter, items started
       auto panel_ready = [&](uint32_t pcx) -> bool {
         return ctl.wait(BAR_RING_FULL + pcx % kRing, (pcx / kRing) & 1u);
@@ -381,35 +387,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Descriptors are built once; a k-step only adds its byte offset >> 4 to the
       // start-address field (every operand lies below 256 KB, so the 14-bit field
       // never carries).
-      const uint64_t dQ0 = ptx::smem_desc(sbase + kOffQ, 16, 1024);
+      const uint64_t dq = ptx::smem_desc(sbase + kOffQ + i * kQBytes, 16, 1024);
       const uint64_t dRingK = ptx::smem_desc(ring, 16, 1024);
       const uint64_t dRingV = ptx::smem_desc(ring, kPanel, 1024);
-      auto issue_qk = [&](int i, uint32_t gg) {
+      const uint32_t d_s = tmem + kColS + 128u * i;  // S_i; P_i aliases its head
+      const uint32_t d_o = tmem + kColO + 128u * i;
+      auto issue_qk = [&](uint32_t gg) {
         const uint32_t s0 = (gg * kPanelsPerTile) % kRing;
-        const uint64_t dq = dQ0 + ((i * kQBytes) >> 4);
-        const uint32_t d = tmem + kColS + 128u * i;
 #pragma unroll
         for (int ks = 0; ks < (kDn + kDr) / 16; ++ks) {
           const uint32_t pn = (uint32_t)(ks >> 2), sub = (uint32_t)(ks & 3) * 32u;
           const uint32_t kslot = (s0 + pn) % kRing;
-          ptx::mma_ss(d, dq + ((pn * kPanel + sub) >> 4), dRingK + ((kslot * kPanel + sub) >> 4), kIdescQK, ks > 0);
+          ptx::mma_ss(d_s, dq + ((pn * kPanel + sub) >> 4), dRingK + ((kslot * kPanel + sub) >> 4), kIdescQK, ks > 0);
         }
         ptx::tc_commit(ctl.bar(BAR_S_FULL + i));
       };
-      auto issue_pv = [&](int i, uint32_t gg, bool first) {
+      auto issue_pv = [&](uint32_t gg, bool first) {
         const uint32_t s0 = (gg * kPanelsPerTile) % kRing;
-        const uint32_t pcol = tmem + kColS + 128u * i;  // P_i aliases the head of S_i
-        const uint32_t d = tmem + kColO + 128u * i;
 #pragma unroll
         for (uint32_t hv = 0; hv < 2; ++hv) {
           const uint64_t dv = dRingV + ((((s0 + 3u + hv) % kRing) * kPanel) >> 4);
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks) {
             // 16 keys: 8 packed P columns; V rows: two 1024-byte groups of 8 keys
-            ptx::mma_ts(d + 64u * hv, pcol + (uint32_t)ks * 8u, dv + (((uint32_t)ks * 2048u) >> 4), kIdescPV,
+            ptx::mma_ts(d_o + 64u * hv, d_s + (uint32_t)ks * 8u, dv + (((uint32_t)ks * 2048u) >> 4), kIdescPV,
                         !(first && ks == 0));
           }
         }
+      };
+      // PV_i of tile gg once P_i and the tile's V panels are there; frees the V panels.
+      auto pv_step = [&](uint32_t gg, bool first) -> bool {
+        const uint32_t vp = gg * kPanelsPerTile + 3u;
+        if (!ctl.wait(BAR_P_FULL + i, gg & 1u) || !panel_ready(vp) || !panel_ready(vp + 1)) return false;
+        ptx::tc_fence_after();
+        issue_pv(gg, first);
+        release(vp);
+        release(vp + 1);
+        return true;
       };
       bool stop = false;
       for (int k = 0; !stop && k * (int)gridDim.x < a.n_items; ++k) {
@@ -429,32 +443,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (;;) {
           const int kn = next_tile(a, it, kt);
           const uint32_t kp = g * kPanelsPerTile;  // first ring panel of tile g
-          if (!first_tile) {  // PV_0 of the previous tile
-            if (!ctl.wait(BAR_P_FULL + 0, (g - 1) & 1u) || !panel_ready(kp - 2) || !panel_ready(kp - 1)) {
+          if (!first_tile) {
+            if (!pv_step(g - 1, first_pv)) {
               stop = true;
               break;
             }
-            ptx::tc_fence_after();
-            issue_pv(0, g - 1, first_pv);
+            first_pv = false;
           }
           if (!panel_ready(kp) || !panel_ready(kp + 1) || !panel_ready(kp + 2)) {
             stop = true;
             break;
           }
           ptx::tc_fence_after();
-          issue_qk(0, g);
-          if (!first_tile) {  // PV_1 of the previous tile; its V panels are then free
-            if (!ctl.wait(BAR_P_FULL + 1, (g - 1) & 1u)) {
-              stop = true;
-              break;
-            }
-            ptx::tc_fence_after();
-            issue_pv(1, g - 1, first_pv);
-            first_pv = false;
-            release(kp - 2);
-            release(kp - 1);
-          }
-          issue_qk(1, g);
+          issue_qk(g);
           release(kp);
           release(kp + 1);
           release(kp + 2);
@@ -464,22 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           kt = kn;
         }
         if (stop) break;
-        ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));  // every QK of this item has been issued
-        // PV of the item's last tile for both halves
-        const uint32_t kp = g * kPanelsPerTile;
-        if (!panel_ready(kp - 2) || !panel_ready(kp - 1)) break;
-        for (int i = 0; i < 2; ++i) {
-          if (!ctl.wait(BAR_P_FULL + i, (g - 1) & 1u)) {
-            stop = true;
-            break;
-          }
-          ptx::tc_fence_after();
-          issue_pv(i, g - 1, first_pv);
-          ptx::tc_commit(ctl.bar(BAR_O_FULL + i));
-        }
-        if (stop) break;
-        release(kp - 2);
-        release(kp - 1);
+        ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));  // every QK of this half has been issued
+        if (!pv_step(g - 1, first_pv)) break;  // PV of the item's last tile
+        ptx::tc_commit(ctl.bar(BAR_O_FULL + i));
       }
       // Drain: every MMA this thread issued has finished before TMEM is released.
       ptx::tc_commit(ctl.bar(BAR_DRAIN));
