@@ -23,7 +23,8 @@
 // registers a thread: 128*120 + 256*192 = 384*168, the launch budget.  Each
 // half's MMAs go out from its own thread in the order
 //   QK_i(j) [softmax_i(j)] PV_i(j) QK_i(j+1) ...
-// so the tensor pipe runs one half's MMAs while the other half's softmax works.
+// so the tensor pipe runs one half's MMAs while the other half's softmax works;
+// half 1 starts each item one softmax later than half 0 so that they alternate.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
 // P_i (bf16 pairs) overwrites the first 64 columns of S_i once they are read,
 // and QK_i(j+1) is issued only after PV_i(j), which the tensor pipe runs in order.
@@ -62,7 +63,8 @@ enum {
   BAR_S_FULL = BAR_RING_EMPTY + kRing,     // 2 (per half)
   BAR_P_FULL = BAR_S_FULL + 2,             // 2
   BAR_O_FULL = BAR_P_FULL + 2,             // 2
-  BAR_DRAIN = BAR_O_FULL + 2,
+  BAR_OFFSET = BAR_O_FULL + 2,             // half 0 finished an item's first tile
+  BAR_DRAIN = BAR_OFFSET + 1,
   kNumBars = BAR_DRAIN + 1
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + 8 * kNumBars;
@@ -312,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ctl.bar(BAR_P_FULL + i), 128);
       ptx::mbar_init(ctl.bar(BAR_O_FULL + i), 1);
     }
+    ptx::mbar_init(ctl.bar(BAR_OFFSET), 128);
     ptx::mbar_init(ctl.bar(BAR_DRAIN), 2);  // both MMA issuers
     *ctl.abort = 0;
     ptx::fence_mbar_init();
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // are released when both halves have committed (their barriers count 2).
     if (lane == 0) {
       const int i = warp - 1;
-      uint32_t g = 0, n_items = 0;  // global tile counter, items started
+      uint32_t g = 0, n_items = 0, n_started = 0;  // global tile counter, items started, items with tiles
       auto panel_ready = [&](uint32_t pcx) -> bool {
         return ctl.wait(BAR_RING_FULL + pcx % kRing, (pcx / kRing) & 1u);
       };
@@ -454,6 +457,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             stop = true;
             break;
           }
+          // Half 1 starts an item only once half 0 has finished softmax of the item's
+          // first tile: the halves then alternate (one half's MMAs under the other
+          // half's softmax) instead of running in lockstep.
+          if (i == 1 && first_tile && !ctl.wait(BAR_OFFSET, n_started & 1u)) {
+            stop = true;
+            break;
+          }
           ptx::tc_fence_after();
           issue_qk(g);
           release(kp);
@@ -465,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           kt = kn;
         }
         if (stop) break;
+        ++n_started;
         ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));  // every QK of this half has been issued
         if (!pv_step(g - 1, first_pv)) break;  // PV of the item's last tile
         ptx::tc_commit(ctl.bar(BAR_O_FULL + i));
@@ -515,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         nhi = S + min(blk * p.bs + p.bs, Qn);
       }
       float m_used = -INFINITY, l = 0.f;
-      bool any_tile = false;
+      bool any_tile = false, any_p = false;
       for (int kt = next_tile(a, it, -1); kt < it.nkt; kt = next_tile(a, it, kt)) {
         any_tile = true;
         const int cls = half_class(a, it.sg, h_has, h_r0, h_r1, h_amin, h_amax, h_cls, kt);
@@ -534,47 +545,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        // pass 1: row maximum over the tile, 64 columns at a time (the scores are
-        // read again in pass 2 rather than held in registers)
-        float mt = -INFINITY;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float x[64];
-          ptx::tmem_ld32(s_col + 64u * hh, reinterpret_cast<uint32_t*>(x));
-          ptx::tmem_ld32(s_col + 64u * hh + 32u, reinterpret_cast<uint32_t*>(x) + 32);
-          ptx::tmem_wait_ld();
-          mask64(x, kind, 64 * hh, pc);
-          mt = fmaxf(mt, max64(x));
-        }
+        // One TMEM read per 64-column half.  p = exp2(x - m) uses the running
+        // reference m (base-2 units) and is packed to bf16 pairs (lower key in the
+        // low half) over the first 64 columns of S, which are already read.  Only
+        // when a half's maximum exceeds m by more than 2^8 -- always on the row's
+        // first visible scores, rarely afterwards -- does m move; everything built
+        // with the old m is then scaled by alpha = exp2(m_old - m_new): O (PV of
+        // the previous tile has completed: it was issued before this tile's QK),
+        // l, and the P columns this tile already wrote.
         const bool scaled = kind == kPrepDense;  // dense scores are already in base-2 units
-        const float m_tile = scaled ? mt : mt * c2;
-        if (m_tile != -INFINITY) {
-          if (m_used == -INFINITY) {
-            m_used = m_tile;  // nothing accumulated for this row yet
-          } else if (m_tile > m_used + 8.0f) {
-            // Rescale O and l to the new maximum.  PV of the previous tile was
-            // issued before this tile's QK, so S_FULL already covers its completion.
-            const float alpha = ptx::ex2(m_used - m_tile);
-#pragma unroll 1
-            for (int cc = 0; cc < kDv; cc += 32) {
-              uint32_t o[32];
-              ptx::tmem_ld32(o_col + cc, o);
-              ptx::tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              ptx::tmem_st32(o_col + cc, o);
-            }
-            ptx::tmem_wait_st();
-            l *= alpha;
-            m_used = m_tile;
-          }
-        }
-        // pass 2: p = exp2(x - m), packed to bf16 pairs (lower key in the low half),
-        // written over the first 64 columns of S; columns 0-63 are re-read before
-        // P overwrites 0-31, and P's 32-63 land on columns already consumed.
-        const float msub = m_used == -INFINITY ? 0.f : m_used;
-        const float2 mul2 = make_float2(scaled ? 1.f : c2, scaled ? 1.f : c2);
-        const float2 neg2 = make_float2(-msub, -msub);
+        const float cm = scaled ? 1.f : c2;
         float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -583,6 +563,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_ld32(s_col + 64u * hh + 32u, reinterpret_cast<uint32_t*>(x) + 32);
           ptx::tmem_wait_ld();
           mask64(x, kind, 64 * hh, pc);
+          const float mh = max64(x) * cm;
+          if (mh > m_used + 8.0f) {  // also when m is still -inf and this half sees a key
+            if (m_used != -INFINITY) {
+              const float alpha = ptx::ex2(m_used - mh);
+#pragma unroll 1
+              for (int cc = 0; cc < kDv; cc += 32) {
+                uint32_t o[32];
+                ptx::tmem_ld32(o_col + cc, o);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                ptx::tmem_st32(o_col + cc, o);
+              }
+              if (hh == 1) {  // P of columns 0-63, written with the old reference
+                uint32_t pr[32];
+                ptx::tmem_wait_st();
+                ptx::tmem_ld32(s_col, pr);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  pr[e] = ptx::pack_bf16x2(__uint_as_float(pr[e] << 16) * alpha,
+                                           __uint_as_float(pr[e] & 0xFFFF0000u) * alpha);
+                ptx::tmem_st32(s_col, pr);
+              }
+              ptx::tmem_wait_st();
+              l *= alpha;
+              lsum.x *= alpha;
+              lsum.y *= alpha;
+            }
+            m_used = mh;
+          }
+          const float msub = m_used == -INFINITY ? 0.f : m_used;
+          const float2 mul2 = make_float2(cm, cm), neg2 = make_float2(-msub, -msub);
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
@@ -597,6 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(ctl.bar(BAR_P_FULL + half));
+        if (half == 0 && !any_p) ptx::mbar_arrive(ctl.bar(BAR_OFFSET));  // lets half 1 start the item
+        any_p = true;
         ++g;
       }
       if (stop) break;
