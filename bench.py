@@ -245,22 +245,35 @@ def run_ours(args):
     import dflash_block_draft_gb300 as dfl
     dfl.load_library()
 
-    d = synth.make(WORKLOAD)
+    workload, dense = args.workload, args.mode == "dense"
+    d = synth.make(workload)
     B, Q, H, S, bs = d["B"], d["Q"], d["H"], d["S"], d["block_size"]
     dn, dr, dv = d["d_nope"], d["d_rope"], d["d_v"]
     work = metrics.anchored_work(d["anchors"], S, Q, H, bs, dn, dr, dv, esize=2)
+    if dense:  # the mask is read once more; visibility is the same as the anchored rule's
+        work["bytes"] += B * Q * (S + Q) * 2 - d["anchors"].size * 4
     host = {k: d[k] for k in ("q", "k_nope", "k_rope", "v")}
     dev = {k: to_dev(v, "bf16", device) for k, v in host.items()}
     anchors = torch.from_numpy(d["anchors"]).to(device)
     out = torch.empty((B, Q, H, dv), dtype=torch.bfloat16, device=device)
-    ws_bytes = dfl.dflash_attn_workspace_size(dfl.MODE_ANCHORED, B, H, S, Q, dn, dr, dv)
+    mode_code = dfl.MODE_DENSE if dense else dfl.MODE_ANCHORED
+    ws_bytes = dfl.dflash_attn_workspace_size(mode_code, B, H, S, Q, dn, dr, dv)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 256 MiB > 129 MB L2
+    mask = None
+    if dense:  # the additive block mask, built on the device from the anchors (+ padding columns)
+        mask = dfl.dflash_build_mask(anchors, bs, S, dtype=torch.bfloat16)
+        if d.get("pad"):
+            mask[:, :, :, S - d["pad"]:S] = float("-inf")
 
     def step():
-        dfl.dflash_attn_anchored(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], anchors, bs, out=out,
-                                 workspace=ws, stream=stream)
+        if dense:
+            dfl.dflash_attn_dense(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], mask, out=out, workspace=ws,
+                                  stream=stream)
+        else:
+            dfl.dflash_attn_anchored(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], anchors, bs, out=out,
+                                     workspace=ws, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -289,16 +302,18 @@ def run_ours(args):
     value = world * work["flops"] / (ms / 1e3) / 1e12
 
     peaks, peak_src = load_peaks()
-    # One kernel per step: the attention kernel is the whole step, so its
-    # average launch duration is the per-step event time.
+    # One kernel per step (anchored): the attention kernel is the whole step, so
+    # its average launch duration is the per-step event time.  The dense entry
+    # point adds the mask scan, whose time is included here.
     kernel_ms = sum(times) / len(times)
     achieved = work["flops"] / (kernel_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     traffic = load_traffic()
 
     # end to end through the public API from pinned host buffers
+    headline = workload == WORKLOAD and not dense
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and headline:
         pinned = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).pin_memory()
                   for k, v in host.items()}
         an_h = torch.from_numpy(d["anchors"]).pin_memory()
@@ -329,7 +344,7 @@ def run_ours(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and headline:
         # The whole workload (every query row, every head), repeated until about
         # 10 s of oracle time has accumulated.
         rows = np.arange(0, B * Q, dtype=np.int64)
@@ -346,12 +361,14 @@ def run_ours(args):
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_desc(d), "l2": "flushed between timed steps (256 MiB write)",
+            "config": {"workload": workload_desc(d) + (" (dense mask entry point)" if dense else ""),
+                       "l2": "flushed between timed steps (256 MiB write)",
                        "unmasked_flops_per_step": work["flops"], "algorithmic_bytes_per_step": work["bytes"],
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": traffic, "peak_source": f"bf16_tflops ({peak_src})",
-                         "kernel": "attention (one launch per step)"},
+                         "frac": achieved / peak, "traffic": traffic if headline else None,
+                         "peak_source": f"bf16_tflops ({peak_src})",
+                         "kernel": "mask scan + attention" if dense else "attention (one launch per step)"},
             "pct_bf16_roofline": 100.0 * achieved / peak,
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": int(launches), "clocks": clocks.summary()}
     if rank == 0:
@@ -454,8 +471,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["prefill_bf16", "decode_bf16"], default="prefill_bf16",
-                    help="prefill_bf16 (the headline) or the ragged decode workload (HBM-bound)")
+    ap.add_argument("--workload", choices=["prefill_bf16", "training_bf16", "long_bf16", "decode_bf16"],
+                    default="prefill_bf16",
+                    help="prefill_bf16 is the headline; the others are the remaining bf16 workloads "
+                         "(decode_bf16 is HBM-bound and reported in GB/s)")
+    ap.add_argument("--mode", choices=["anchored", "dense"], default="anchored",
+                    help="entry point for the batched workloads")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

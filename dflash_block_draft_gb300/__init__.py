@@ -33,7 +33,7 @@ STATUS = {0: "DFLASH_OK", 1: "DFLASH_ERR_INVALID", 2: "DFLASH_ERR_SHAPE", 3: "DF
 
 EXPORTS = ("dflash_attn_dense", "dflash_attn_anchored", "dflash_attn_ragged", "dflash_attn_workspace_size",
            "dflash_build_schedule_host", "dflash_scan_mask", "dflash_status_string", "dflash_last_device_error",
-           "dflash_kernel_launches", "dflash_attn_dense_noalloc")
+           "dflash_kernel_launches", "dflash_attn_dense_noalloc", "dflash_build_mask")
 
 
 class DFlashError(RuntimeError):
@@ -76,6 +76,8 @@ def load_library(path: str | None = None):
         lib.dflash_status_string.restype = ctypes.c_char_p
         lib.dflash_last_device_error.argtypes = [P]
         lib.dflash_attn_dense_noalloc.argtypes = [DP, I, P, P, P, P, P, P, P, P]
+        lib.dflash_build_mask.argtypes = [I, I, I, P, I, I, I, P, P]
+        lib.dflash_build_mask.restype = ctypes.c_int
         lib.dflash_attn_dense_noalloc.restype = ctypes.c_int
         lib.dflash_kernel_launches.argtypes = []
         lib.dflash_kernel_launches.restype = ctypes.c_uint64
@@ -278,6 +280,22 @@ def dflash_build_schedule_host(B, S, Q, anchors, block_size) -> np.ndarray:
                                         out.ctypes.data_as(ctypes.c_void_p))
     _check("dflash_build_schedule_host", st)
     return out
+
+
+def dflash_build_mask(anchors, block_size, S, dtype=None, mask=None, stream=None):
+    """Device additive mask [B,1,Q,S+Q] (0 visible, -inf hidden) of the anchored
+    rule from anchors [B,nb] int32 (CUDA).  dtype: torch.bfloat16 or torch.float32."""
+    torch = _torch()
+    lib = load_library()
+    B, nb = anchors.shape
+    Q = nb * int(block_size)
+    dtype = dtype or torch.bfloat16
+    if mask is None:
+        mask = torch.empty((B, 1, Q, S + Q), dtype=dtype, device=anchors.device)
+    st = lib.dflash_build_mask(B, S, Q, _dev_ptr(anchors, "anchors", torch.int32), nb, int(block_size),
+                               _dtype_code(mask), _dev_ptr(mask, "mask"), _stream(stream))
+    _check("dflash_build_mask", st)
+    return mask
 
 
 def dflash_scan_mask(mask, classes=None, stream=None):

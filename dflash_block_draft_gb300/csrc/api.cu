@@ -228,6 +228,18 @@ dflash_status_t dflash_scan_mask(int B, int S, int Q, dflash_dtype_t dtype, cons
   return launched(launch_mask_scan(mask, dtype == DFLASH_BF16, B, S, Q, classes, (cudaStream_t)stream));
 }
 
+dflash_status_t dflash_build_mask(int B, int S, int Q, const int32_t* anchors, int nb, int block_size,
+                                  dflash_dtype_t dtype, void* mask, dflash_stream_t stream) {
+  if (check_dtype(dtype) != DFLASH_OK) return DFLASH_ERR_DTYPE;
+  if (B < 0 || S < 0 || Q < 0 || nb < 0 || block_size <= 0 || (long long)nb * block_size != Q)
+    return DFLASH_ERR_SHAPE;
+  if ((long long)S + Q >= (1ll << 31) || Q > (1 << 30) || B > 65535) return DFLASH_ERR_UNSUPPORTED;
+  if (B == 0 || Q == 0) return DFLASH_OK;
+  if (!anchors || !mask) return DFLASH_ERR_INVALID;
+  return launched(launch_build_mask(anchors, dtype == DFLASH_BF16, B, S, Q, nb, block_size, mask, error_word(),
+                                    (cudaStream_t)stream));
+}
+
 dflash_status_t dflash_attn_dense(const dflash_dims_t* dims, dflash_dtype_t dtype, const void* q,
                                   const void* k_nope, const void* k_rope, const void* v, const void* mask,
                                   void* out, float* lse, void* workspace, size_t ws_bytes,

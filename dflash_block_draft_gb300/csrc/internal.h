@@ -64,6 +64,8 @@ int decode_max_units(int R, int total_kv);
 size_t decode_workspace_bytes(int R, int H, int total_kv);
 cudaError_t launch_attn_decode(const AttnParams& p, void* ws, cudaStream_t stream);
 
+cudaError_t launch_build_mask(const int32_t* anchors, bool bf16, int B, int S, int Q, int nb, int bs, void* mask,
+                              unsigned* err, cudaStream_t stream);
 cudaError_t launch_mask_scan(const void* mask, bool bf16, int B, int S, int Q, uint8_t* classes,
                              cudaStream_t stream);
 

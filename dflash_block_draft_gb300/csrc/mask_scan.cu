@@ -82,7 +82,40 @@ __global__ void __launch_bounds__(kScanThreads) mask_scan_kernel(const void* __r
   }
 }
 
+// The additive DFlash block mask of the anchored rule: row i of batch row b
+// (block j = i / bs) is 0 on context keys p < a_j and on its own block's noise
+// keys, -inf elsewhere.  One CTA per (row, batch row); 16-byte stores.
+template <bool kBf16>
+__global__ void __launch_bounds__(256) build_mask_kernel(const int32_t* __restrict__ anchors, int S, int Q, int nb,
+                                                         int bs, void* __restrict__ mask, unsigned* err) {
+  const int i = blockIdx.x, b = blockIdx.y;
+  const int K = S + Q;
+  int a = anchors[(size_t)b * nb + i / bs];
+  if (a < 0 || a > S) {
+    if (threadIdx.x == 0) record_error(err, DFLASH_ERR_INVALID);
+    a = a < 0 ? 0 : S;
+  }
+  const int blk = i / bs;
+  const int nlo = S + blk * bs, nhi = S + min(blk * bs + bs, Q);
+  const size_t row = ((size_t)b * Q + i) * (size_t)K;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    const bool vis = k < a || (k >= nlo && k < nhi);
+    if (kBf16) static_cast<uint16_t*>(mask)[row + k] = vis ? 0u : 0xFF80u;
+    else static_cast<uint32_t*>(mask)[row + k] = vis ? 0u : 0xFF800000u;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_build_mask(const int32_t* anchors, bool bf16, int B, int S, int Q, int nb, int bs, void* mask,
+                              unsigned* err, cudaStream_t stream) {
+  if (B == 0 || Q == 0) return cudaSuccess;
+  const dim3 grid(Q, B);
+  if (bf16) build_mask_kernel<true><<<grid, 256, 0, stream>>>(anchors, S, Q, nb, bs, mask, err);
+  else build_mask_kernel<false><<<grid, 256, 0, stream>>>(anchors, S, Q, nb, bs, mask, err);
+  count_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_mask_scan(const void* mask, bool bf16, int B, int S, int Q, uint8_t* classes,
                              cudaStream_t stream) {

@@ -222,6 +222,20 @@ DFLASH_API dflash_status_t dflash_scan_mask(int B, int S, int Q, dflash_dtype_t 
  */
 DFLASH_API uint64_t dflash_kernel_launches(void);
 
+/*
+ * Builds the additive DFlash block mask of the anchored rule on the device:
+ * mask [B, 1, Q, S+Q] of dtype gets 0 where row i (block j = i/block_size) may
+ * attend -- context keys p < anchors[b, j] and the block_size noise keys of
+ * block j -- and -inf everywhere else.  This is the dense mask the trainer
+ * hands the draft (nemo_automodel.components.speculative.dflash.draft_kimi_k3
+ * page, module docstring: the block structure is supplied entirely by the
+ * attention mask; KimiK3DFlashAttention.forward: its shape).  anchors [B, nb]
+ * int32 on the device; anchors outside [0, S] are clamped and recorded as
+ * DFLASH_ERR_INVALID in the device error word.  Asynchronous on `stream`.
+ */
+DFLASH_API dflash_status_t dflash_build_mask(int B, int S, int Q, const int32_t* anchors, int nb, int block_size,
+                                             dflash_dtype_t dtype, void* mask, dflash_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 DFLASH_API const char* dflash_status_string(dflash_status_t status);
 

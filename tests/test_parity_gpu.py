@@ -153,6 +153,17 @@ def test_mask_scan_bit_exact_vs_bruteforce(dfl):
         np.testing.assert_array_equal(got, want)
 
 
+@pytest.mark.parametrize("dtype,S,nb,bs", [("bf16", 300, 23, 8), ("fp32", 1000, 30, 12), ("bf16", 4096, 256, 16)])
+def test_device_mask_builder_bit_exact_vs_oracle(dfl, dtype, S, nb, bs):
+    d = _small_case(dtype, 2, 1, S, nb, bs, 8, 8, 8, seed=S + nb)
+    d["anchors"][0, 0] = 0
+    d["anchors"][-1, -1] = S
+    want = oracle.build_mask(d["anchors"], bs, S)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    got = dfl.dflash_build_mask(torch.from_numpy(d["anchors"]).cuda(), bs, S, dtype=tdt).float().cpu().numpy()
+    np.testing.assert_array_equal(got, want)
+
+
 def test_outputs_fully_written_and_guard_bands_untouched(dfl):
     d = _small_case("bf16", 1, 2, 260, 13, 8, 128, 64, 128, seed=13)
     t = _dev(d, "bf16")
