@@ -24,7 +24,7 @@
 // half's MMAs go out from its own thread in the order
 //   QK_i(j) [softmax_i(j)] PV_i(j) QK_i(j+1) ...
 // so the tensor pipe runs one half's MMAs while the other half's softmax works;
-// half 1 starts each item one softmax later than half 0 so that they alternate.
+// half 1 starts one softmax later than half 0 so that they alternate.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
 // P_i (bf16 pairs) overwrites the first 64 columns of S_i once they are read,
 // and QK_i(j+1) is issued only after PV_i(j), which the tensor pipe runs in order.
@@ -457,10 +457,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             stop = true;
             break;
           }
-          // Half 1 starts an item only once half 0 has finished softmax of the item's
-          // first tile: the halves then alternate (one half's MMAs under the other
-          // half's softmax) instead of running in lockstep.
-          if (i == 1 && first_tile && !ctl.wait(BAR_OFFSET, n_started & 1u)) {
+          // Half 1 starts the CTA's first item only once half 0 has finished softmax
+          // of its first tile: the halves then alternate (one half's MMAs under the
+          // other half's softmax) instead of running in lockstep.  Later items keep
+          // the offset by themselves (half 1 finishes each item later).
+          if (i == 1 && first_tile && n_started == 0 && !ctl.wait(BAR_OFFSET, 0)) {
             stop = true;
             break;
           }
@@ -610,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(ctl.bar(BAR_P_FULL + half));
-        if (half == 0 && !any_p) ptx::mbar_arrive(ctl.bar(BAR_OFFSET));  // lets half 1 start the item
+        if (half == 0 && !any_p && n_full == 0) ptx::mbar_arrive(ctl.bar(BAR_OFFSET));  // lets half 1 start
         any_p = true;
         ++g;
       }
