@@ -387,7 +387,7 @@ def run_decode(args):
     device = torch.device("cuda", 0)
     import dflash_block_draft_gb300 as dfl
     dfl.load_library()
-    d = synth.make("decode_bf16")
+    d = synth.make("decode_bf16", **({"R": args.requests} if args.requests else {}))
     H, bs = d["H"], d["block_size"]
     work = metrics.ragged_work(d["q_offsets"], d["kv_offsets"], d["anchors"], H, bs, d["d_nope"], d["d_rope"],
                                d["d_v"])
@@ -477,6 +477,9 @@ def main(argv=None):
                          "(decode_bf16 is HBM-bound and reported in GB/s)")
     ap.add_argument("--mode", choices=["anchored", "dense"], default="anchored",
                     help="entry point for the batched workloads")
+    ap.add_argument("--requests", type=int, default=None,
+                    help="decode_bf16 only: draw this many requests instead of 64 (same recipe; "
+                         "for profiling captures that must stay small)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
