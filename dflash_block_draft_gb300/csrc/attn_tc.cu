@@ -23,15 +23,19 @@
 // registers a thread: 128*120 + 256*192 = 384*168, the launch budget.  Each
 // half's MMAs go out from its own thread in the order
 //   QK_i(j) [softmax_i(j)] PV_i(j) QK_i(j+1) ...
-// so the tensor pipe runs one half's MMAs while the other half's softmax works;
-// half 1 starts one softmax later than half 0 so that they alternate.
+// (PV_i(j) and QK_i(j+1) back to back once P_i(j) is there).  Left free, the
+// two issue streams interleave in the tensor pipe and the halves run in step;
+// making them take turns would let one half's softmax overlap the other half's
+// MMAs, but then the ring must hold two key tiles per half, more than fits.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
 // P_i (bf16 pairs) overwrites the first 64 columns of S_i once they are read,
 // and QK_i(j+1) is issued only after PV_i(j), which the tensor pipe runs in order.
 // Shared memory: both Q tiles (96 KB) and a ring of eight 16 KB panels through
-// which the K tiles (nope 0-63, nope 64-127, rope: 3 panels) and V tiles
-// (v 0-63, v 64-127: 2 panels) stream in consumption order, all in the
-// 128-byte-swizzled layout TMA writes.
+// which each key tile streams as five panels, all in the 128-byte-swizzled
+// layout TMA writes: K (nope 0-63, nope 64-127, rope) then V (v 0-63,
+// v 64-127).  PV runs as N = 128 MMAs, which need the two V panels adjacent;
+// for the one tile in eight whose V pair would wrap around the ring's end, the
+// tile's panels are stored V first (see v_first).
 // The grid is persistent (one CTA per SM); items are dealt in a snake order over
 // a longest-first list (query tiles with the most context first).
 // Every mbarrier wait is bounded; a wait that runs past its budget records
@@ -63,8 +67,7 @@ enum {
   BAR_S_FULL = BAR_RING_EMPTY + kRing,     // 2 (per half)
   BAR_P_FULL = BAR_S_FULL + 2,             // 2
   BAR_O_FULL = BAR_P_FULL + 2,             // 2
-  BAR_OFFSET = BAR_O_FULL + 2,             // half 0 finished an item's first tile
-  BAR_DRAIN = BAR_OFFSET + 1,
+  BAR_DRAIN = BAR_O_FULL + 2,
   kNumBars = BAR_DRAIN + 1
 };
 constexpr uint32_t kOffTmemSlot = kOffBar + 8 * kNumBars;
@@ -83,7 +86,15 @@ constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s per wait
 constexpr uint32_t kSleepHintNs = 100000;           // re-check the budget every ~0.1 ms of sleep
 
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBM, kBN, 0, 0);  // Q, K both K-major
-constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, 64, 0, 1);   // P from TMEM, V MN-major, 64 columns
+constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, kDv, 0, 1);  // P from TMEM, V MN-major (both panels)
+
+// Ring placement of key tile g (counted over the CTA's whole run): its panels
+// are ring slots (5g .. 5g+4) mod 8.  Normally K takes the first three and V the
+// last two; when those two would be slots 7 and 0, V takes the first two
+// instead, so that V always occupies two adjacent slots.
+__device__ __forceinline__ bool v_first(uint32_t g) { return (g * kPanelsPerTile + 3u) % kRing == kRing - 1u; }
+__device__ __forceinline__ uint32_t k_panel0(uint32_t g) { return g * kPanelsPerTile + (v_first(g) ? 2u : 0u); }
+__device__ __forceinline__ uint32_t v_panel0(uint32_t g) { return g * kPanelsPerTile + (v_first(g) ? 0u : 3u); }
 
 struct TcArgs {
   AttnParams p;
@@ -132,11 +143,20 @@ __device__ __forceinline__ Item decode_item(const TcArgs& a, int idx) {
     if (p.mode == kDense) {
       it.cls[i] = p.classes + ((long long)it.z * p.nqt + t) * p.nkt;
     } else {
-      for (int j = it.r0[i] / p.bs; j <= (it.r1[i] - 1) / p.bs; ++j) {
-        int an = p.anchors[it.sg.anc0 + j];
-        an = an < 0 ? 0 : (an > S ? S : an);
-        it.amin[i] = min(it.amin[i], an);
-        it.amax[i] = max(it.amax[i], an);
+      // The tile's anchors, eight independent loads at a time (a load-use chain
+      // per anchor would cost one memory latency each).
+      const int j0 = it.r0[i] / p.bs, j1 = (it.r1[i] - 1) / p.bs;
+      const int* ap = p.anchors + it.sg.anc0;
+      for (int jb = j0; jb <= j1; jb += 8) {
+        int an[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) an[u] = __ldg(ap + min(jb + u, j1));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int c = an[u] < 0 ? 0 : (an[u] > S ? S : an[u]);
+          it.amin[i] = min(it.amin[i], c);
+          it.amax[i] = max(it.amax[i], c);
+        }
       }
     }
   }
@@ -314,7 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ctl.bar(BAR_P_FULL + i), 128);
       ptx::mbar_init(ctl.bar(BAR_O_FULL + i), 1);
     }
-    ptx::mbar_init(ctl.bar(BAR_OFFSET), 128);
     ptx::mbar_init(ctl.bar(BAR_DRAIN), 2);  // both MMA issuers
     *ctl.abort = 0;
     ptx::fence_mbar_init();
@@ -358,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++n_items;
         for (int kt = next_tile(a, it, -1); kt < it.nkt && !stop; kt = next_tile(a, it, kt)) {
           const int krow = (int)(it.sg.kv0 + (long long)kt * kBN);
+          const bool vf = v_first(pc / kPanelsPerTile);
           for (uint32_t pn = 0; pn < kPanelsPerTile; ++pn, ++pc) {
             const uint32_t s = pc % kRing;
             if (!ctl.wait(BAR_RING_EMPTY + s, ((pc / kRing) & 1u) ^ 1u)) {
@@ -367,9 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = ring + s * kPanel;
             const uint32_t fb = ctl.bar(BAR_RING_FULL + s);
             ptx::mbar_arrive_expect_tx(fb, kPanel);
-            if (pn < 2) ptx::tma_load_3d(dst, &tmKn, fb, 64 * pn, it.h, krow);
-            else if (pn == 2) ptx::tma_load_2d(dst, &tmKr, fb, 0, krow);
-            else ptx::tma_load_3d(dst, &tmV, fb, 64 * (pn - 3), it.h, krow);
+            // role: 0, 1 k_nope halves; 2 k_rope; 3, 4 v halves
+            const uint32_t role = vf ? (pn < 2 ? pn + 3 : pn - 2) : pn;
+            if (role < 2) ptx::tma_load_3d(dst, &tmKn, fb, 64 * role, it.h, krow);
+            else if (role == 2) ptx::tma_load_2d(dst, &tmKr, fb, 0, krow);
+            else ptx::tma_load_3d(dst, &tmV, fb, 64 * (role - 3), it.h, krow);
           }
         }
       }
@@ -382,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // are released when both halves have committed (their barriers count 2).
     if (lane == 0) {
       const int i = warp - 1;
-      uint32_t g = 0, n_items = 0, n_started = 0;  // global tile counter, items started, items with tiles
+      uint32_t g = 0, n_items = 0;  // global tile counter, items started
       auto panel_ready = [&](uint32_t pcx) -> bool {
         return ctl.wait(BAR_RING_FULL + pcx % kRing, (pcx / kRing) & 1u);
       };
@@ -396,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t d_s = tmem + kColS + 128u * i;  // S_i; P_i aliases its head
       const uint32_t d_o = tmem + kColO + 128u * i;
       auto issue_qk = [&](uint32_t gg) {
-        const uint32_t s0 = (gg * kPanelsPerTile) % kRing;
+        const uint32_t s0 = k_panel0(gg);
 #pragma unroll
         for (int ks = 0; ks < (kDn + kDr) / 16; ++ks) {
           const uint32_t pn = (uint32_t)(ks >> 2), sub = (uint32_t)(ks & 3) * 32u;
@@ -406,27 +428,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_commit(ctl.bar(BAR_S_FULL + i));
       };
       auto issue_pv = [&](uint32_t gg, bool first) {
-        const uint32_t s0 = (gg * kPanelsPerTile) % kRing;
+        const uint64_t dv = dRingV + (((v_panel0(gg) % kRing) * kPanel) >> 4);
 #pragma unroll
-        for (uint32_t hv = 0; hv < 2; ++hv) {
-          const uint64_t dv = dRingV + ((((s0 + 3u + hv) % kRing) * kPanel) >> 4);
-#pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks) {
-            // 16 keys: 8 packed P columns; V rows: two 1024-byte groups of 8 keys
-            ptx::mma_ts(d_o + 64u * hv, d_s + (uint32_t)ks * 8u, dv + (((uint32_t)ks * 2048u) >> 4), kIdescPV,
-                        !(first && ks == 0));
-          }
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          // 16 keys: 8 packed P columns; V rows: two 1024-byte groups of 8 keys;
+          // the 128 output columns span both V panels (LBO = one panel)
+          ptx::mma_ts(d_o, d_s + (uint32_t)ks * 8u, dv + (((uint32_t)ks * 2048u) >> 4), kIdescPV,
+                      !(first && ks == 0));
         }
       };
-      // PV_i of tile gg once P_i and the tile's V panels are there; frees the V panels.
-      auto pv_step = [&](uint32_t gg, bool first) -> bool {
-        const uint32_t vp = gg * kPanelsPerTile + 3u;
-        if (!ctl.wait(BAR_P_FULL + i, gg & 1u) || !panel_ready(vp) || !panel_ready(vp + 1)) return false;
-        ptx::tc_fence_after();
+      // Waits for tile gg's V panels and P_i (the panels are normally in place long
+      // before P_i, so that the MMAs go out right after P_i arrives).
+      auto pv_ready = [&](uint32_t gg) -> bool {
+        const uint32_t vp = v_panel0(gg);
+        return panel_ready(vp) && panel_ready(vp + 1) && ctl.wait(BAR_P_FULL + i, gg & 1u);
+      };
+      auto pv_issue = [&](uint32_t gg, bool first) {
+        const uint32_t vp = v_panel0(gg);
         issue_pv(gg, first);
         release(vp);
         release(vp + 1);
-        return true;
       };
       bool stop = false;
       for (int k = 0; !stop && k * (int)gridDim.x < a.n_items; ++k) {
@@ -441,31 +462,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));
           continue;
         }
-        ptx::tc_fence_after();
         bool first_tile = true, first_pv = true;
         for (;;) {
           const int kn = next_tile(a, it, kt);
-          const uint32_t kp = g * kPanelsPerTile;  // first ring panel of tile g
-          if (!first_tile) {
-            if (!pv_step(g - 1, first_pv)) {
-              stop = true;
-              break;
-            }
-            first_pv = false;
-          }
-          if (!panel_ready(kp) || !panel_ready(kp + 1) || !panel_ready(kp + 2)) {
-            stop = true;
-            break;
-          }
-          // Half 1 starts the CTA's first item only once half 0 has finished softmax
-          // of its first tile: the halves then alternate (one half's MMAs under the
-          // other half's softmax) instead of running in lockstep.  Later items keep
-          // the offset by themselves (half 1 finishes each item later).
-          if (i == 1 && first_tile && n_started == 0 && !ctl.wait(BAR_OFFSET, 0)) {
+          const uint32_t kp = k_panel0(g);  // first K panel of tile g
+          // The K panels never wait on this half's PV of tile g-1: the ring slots they
+          // reuse were freed by MMAs of tiles g-2 and earlier, or by QK of tile g-1.
+          if (!panel_ready(kp) || !panel_ready(kp + 1) || !panel_ready(kp + 2) || (!first_tile && !pv_ready(g - 1))) {
             stop = true;
             break;
           }
           ptx::tc_fence_after();
+          if (!first_tile) {
+            pv_issue(g - 1, first_pv);
+            first_pv = false;
+          }
           issue_qk(g);
           release(kp);
           release(kp + 1);
@@ -476,9 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           kt = kn;
         }
         if (stop) break;
-        ++n_started;
         ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));  // every QK of this half has been issued
-        if (!pv_step(g - 1, first_pv)) break;  // PV of the item's last tile
+        if (!pv_ready(g - 1)) break;  // PV of the item's last tile
+        ptx::tc_fence_after();
+        pv_issue(g - 1, first_pv);
         ptx::tc_commit(ctl.bar(BAR_O_FULL + i));
       }
       // Drain: every MMA this thread issued has finished before TMEM is released.
@@ -527,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         nhi = S + min(blk * p.bs + p.bs, Qn);
       }
       float m_used = -INFINITY, l = 0.f;
-      bool any_tile = false, any_p = false;
+      bool any_tile = false;
       for (int kt = next_tile(a, it, -1); kt < it.nkt; kt = next_tile(a, it, kt)) {
         any_tile = true;
         const int cls = half_class(a, it.sg, h_has, h_r0, h_r1, h_amin, h_amax, h_cls, kt);
@@ -611,8 +623,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(ctl.bar(BAR_P_FULL + half));
-        if (half == 0 && !any_p && n_full == 0) ptx::mbar_arrive(ctl.bar(BAR_OFFSET));  // lets half 1 start
-        any_p = true;
         ++g;
       }
       if (stop) break;
