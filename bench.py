@@ -163,6 +163,13 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def job_value(units_per_rank: float, world: int, max_ms: float) -> float:
+    """Whole-job throughput in units per second.  Every rank runs the same
+    workload (replicas, weak scaling), so the job processes world x the units of
+    one rank in the time of the slowest rank."""
+    return world * units_per_rank / (max_ms / 1e3)
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -299,7 +306,7 @@ def run_ours(args):
     launches = dfl.dflash_kernel_launches() - launches0
     times = [a.elapsed_time(b) for a, b in ev]
     ms = max_over_ranks(sum(times) / len(times), world, device)
-    value = world * work["flops"] / (ms / 1e3) / 1e12
+    value = job_value(work["flops"], world, ms) / 1e12
 
     peaks, peak_src = load_peaks()
     # One kernel per step (anchored): the attention kernel is the whole step, so
@@ -340,7 +347,7 @@ def run_ours(args):
             ee[k][1].record(stream)
         torch.cuda.synchronize(device)
         e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ee) / args.steps, world, device)
-        e2e = {"value": world * work["flops"] / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_value(work["flops"], world, e_ms) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms}
 
     cpu = None
@@ -436,28 +443,36 @@ def run_decode(args):
                                    f"total_kv={d['total_kv']}", "l2": "flushed between timed steps (256 MiB write)",
                        "algorithmic_bytes_per_step": work["bytes"], "unmasked_flops_per_step": work["flops"]},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                         "traffic": None, "peak_source": f"hbm_gbs ({src})",
-                         "kernel": "plan + split attention + combine (one step)"},
+                         "traffic": load_traffic("decode_bf16", work["bytes"]), "peak_source": f"hbm_gbs ({src})",
+                         "kernel": "plan + split attention + combine (one step; the attention kernel is 95 % of it)",
+                         "traffic_note": "attn_decode_kernel DRAM bytes from a 16-request capture, scaled by "
+                                         "algorithmic bytes"},
             "gpu_launches": int(launches), "clocks": clocks.summary()}
     print(json.dumps(line), flush=True)
     return 0
 
 
-def load_traffic():
+def load_traffic(key=None, alg_bytes=None):
     """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, when it was taken on the kernel source as it is now; else None."""
+    summary, when it was taken on the kernel source as it is now; else None.
+    A capture of a smaller case of the same recipe is scaled to this launch by
+    its algorithmic bytes (traffic grows in proportion)."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         with open(p) as f:
-            t = json.load(f).get(WORKLOAD)
+            t = json.load(f).get(key or WORKLOAD)
         if not t:
             return None
         with open(os.path.join(ROOT, t["source"]), "rb") as f:
             if hashlib.md5(f.read()).hexdigest() != t["source_md5"]:
                 return None  # kernel changed since the counters were taken
+        if "algorithmic_bytes_of_capture" in t:
+            if not alg_bytes:
+                return None
+            return int(round(t["bytes_per_launch"] * alg_bytes / t["algorithmic_bytes_of_capture"]))
         return int(t["bytes_per_launch"])
     except Exception:
         return None
