@@ -156,6 +156,25 @@ bool use_tc(dflash_dtype_t dtype, int dn, int dr, int dv, long long q_rows, long
   return !env_flag("DFLASH_FORCE_SIMT");
 }
 
+// Two tensor-core kernels compute the same result.  attn_tc2.cu (CTA pairs,
+// items of four query tiles) alternates the two halves of an item on the
+// tensor pipe and wins on long contexts; attn_tc.cu (one CTA, items of two
+// query tiles) has less masked work per item and finer load balance, and wins
+// on short ones.  The switch is at 16384 keys per segment on average (measured
+// on GB300, anchored: S+Q = 8192 favours attn_tc.cu by 13 %, 16384 is even,
+// 34816 favours the pair kernel by 10 %).  Dense masks stay on attn_tc.cu: the
+// pair kernel's per-tile class lookups over four query tiles cost it 10-25 %.
+// DFLASH_TC_KERNEL=1 or 2 forces one.
+cudaError_t launch_tc(const AttnParams& p, int segments, int nqt, long long q_rows, long long kv_rows,
+                      cudaStream_t stream) {
+  const char* force = getenv("DFLASH_TC_KERNEL");
+  bool pair = p.mode != kDense && segments > 0 && kv_rows / segments >= 16384;
+  if (force && force[0] == '1') pair = false;
+  if (force && force[0] == '2') pair = true;
+  if (pair) return launch_attn_tc2(p, segments, nqt, q_rows, kv_rows, stream);
+  return launch_attn_tc(p, segments, nqt, q_rows, kv_rows, stream);
+}
+
 }  // namespace
 }  // namespace dflash
 
@@ -270,7 +289,7 @@ dflash_status_t dflash_attn_dense(const dflash_dims_t* dims, dflash_dtype_t dtyp
   p.nkt = (dims->S + dims->Q + kTileN - 1) / kTileN;
   const long long q_rows = (long long)dims->B * dims->Q, kv_rows = (long long)dims->B * (dims->S + dims->Q);
   if (use_tc(dtype, dims->d_nope, dims->d_rope, dims->d_v, q_rows, kv_rows))
-    return launched(launch_attn_tc(p, dims->B, p.nqt, q_rows, kv_rows, s));
+    return launched(launch_tc(p, dims->B, p.nqt, q_rows, kv_rows, s));
   return launched(launch_attn_simt(p, bf16, dims->B, dims->Q, s));
 }
 
@@ -298,7 +317,7 @@ dflash_status_t dflash_attn_anchored(const dflash_dims_t* dims, dflash_dtype_t d
   p.anchors = anchors;
   const long long q_rows = (long long)dims->B * dims->Q, kv_rows = (long long)dims->B * (dims->S + dims->Q);
   if (use_tc(dtype, dims->d_nope, dims->d_rope, dims->d_v, q_rows, kv_rows))
-    return launched(launch_attn_tc(p, dims->B, (dims->Q + kTileM - 1) / kTileM, q_rows, kv_rows,
+    return launched(launch_tc(p, dims->B, (dims->Q + kTileM - 1) / kTileM, q_rows, kv_rows,
                                    (cudaStream_t)stream));
   return launched(launch_attn_simt(p, dtype == DFLASH_BF16, dims->B, dims->Q, (cudaStream_t)stream));
 }
@@ -334,7 +353,7 @@ dflash_status_t dflash_attn_ragged(int R, int H, int d_nope, int d_rope, int d_v
   if (decode && (long long)total_q + kTileM < (1ll << 31) && (long long)total_kv + kTileN < (1ll << 31))
     return launched(launch_attn_decode(p, static_cast<uint8_t*>(workspace) + kAlign, (cudaStream_t)stream));
   if (use_tc(dtype, d_nope, d_rope, d_v, total_q, total_kv))
-    return launched(launch_attn_tc(p, R, (max_q_len + kTileM - 1) / kTileM, total_q, total_kv,
+    return launched(launch_tc(p, R, (max_q_len + kTileM - 1) / kTileM, total_q, total_kv,
                                    (cudaStream_t)stream));
   return launched(launch_attn_simt(p, dtype == DFLASH_BF16, R, max_q_len, (cudaStream_t)stream));
 }

@@ -74,14 +74,17 @@ def _small_case(dtype, B, H, S, nb, bs, dn, dr, dv, seed=123):
                       d_rope=dr, d_v=dv, anchor_lo=0, anchor_hi=S + 1)
 
 
-@pytest.fixture(params=["default", "simt"])
+@pytest.fixture(params=["default", "simt", "tc1", "tc2"])
 def kernel(request, monkeypatch):
     """Run a case on the default dispatch (tensor cores for the Kimi K3 MLA bf16
-    shape) and again with the exact CUDA-core kernel forced."""
+    shape), with the exact CUDA-core kernel forced, and with each of the two
+    tensor-core kernels (one CTA per item; CTA pairs) forced."""
+    monkeypatch.delenv("DFLASH_FORCE_SIMT", raising=False)
+    monkeypatch.delenv("DFLASH_TC_KERNEL", raising=False)
     if request.param == "simt":
         monkeypatch.setenv("DFLASH_FORCE_SIMT", "1")
-    else:
-        monkeypatch.delenv("DFLASH_FORCE_SIMT", raising=False)
+    elif request.param in ("tc1", "tc2"):
+        monkeypatch.setenv("DFLASH_TC_KERNEL", request.param[-1])
     return request.param
 
 
@@ -314,8 +317,12 @@ def _lse_rows_batched(got_l, d, rows):
     return got_l[b, :, i]
 
 
-@pytest.mark.parametrize("name", ["prefill_bf16", "training_bf16", "long_bf16"])
-def test_full_workload_anchored_sampled(dfl, name):
+@pytest.mark.parametrize("name,tc", [("prefill_bf16", None), ("training_bf16", None), ("long_bf16", None),
+                                     ("prefill_bf16", "2"), ("long_bf16", "1")])
+def test_full_workload_anchored_sampled(dfl, name, tc, monkeypatch):
+    # default dispatch on every workload, then each workload size on the kernel it does not pick by default
+    if tc:
+        monkeypatch.setenv("DFLASH_TC_KERNEL", tc)
     d = synth.make(name)
     got_o, got_l = _run_batched(dfl, d, "anchored", "bf16")
     assert not np.isnan(got_o).any()
