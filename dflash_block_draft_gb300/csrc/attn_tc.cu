@@ -457,6 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         else kind = p.mode == kDense ? kPrepDense : kPrepAnchored;
         const PrepCtx pc{ctx_lim - k0, nlo - k0, nhi - k0, mrow ? mrow + k0 : nullptr, K - k0,
                          a.mask_vec != 0, c2};
+        if (kind == kPrepDense) {
+          // The row's 256 mask bytes of this tile go to L1 while S is computed.
+          const char* mp = reinterpret_cast<const char*>(pc.mask);
+          const int span = min(K - k0, kBN) * 2;
+          ptx::prefetch_l1(mp);
+          ptx::prefetch_l1(mp + min(128, span - 1));
+          ptx::prefetch_l1(mp + span - 1);
+        }
         if (!ctl.wait(BAR_S_FULL + half, g & 1u)) {
           stop = true;
           break;

@@ -12,7 +12,7 @@
 namespace dflash {
 namespace {
 
-constexpr int kScanThreads = 256;  // 2 threads per tile row, 64 keys each
+constexpr int kScanThreads = 128;  // one CTA per tile: a 2048-tile mask fits in one wave
 
 __device__ __forceinline__ void classify_bits(uint32_t bits, bool is_bf16, bool& zero, bool& neginf) {
   if (is_bf16) {
@@ -30,38 +30,45 @@ __global__ void __launch_bounds__(kScanThreads) mask_scan_kernel(const void* __r
                                                                  uint8_t* __restrict__ classes) {
   const int kt = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
   const int K = S + Q;
-  const int row = qt * kTileM + (threadIdx.x >> 1);
-  const int c0 = kt * kTileN + (threadIdx.x & 1) * (kTileN / 2);
-  const int c1 = min(c0 + kTileN / 2, K);
+  const int r0 = qt * kTileM, c0 = kt * kTileN;
+  const int c1 = min(c0 + kTileN, K);
   bool all_zero = true, all_ninf = true;
-  if (row < Q && c0 < c1) {
-    const size_t base = ((size_t)b * Q + row) * (size_t)K;
-    if (vec_ok && c1 - c0 == kTileN / 2) {
-      // 64 keys = 128 B (bf16) or 256 B (fp32) as 16-byte vectors.
-      constexpr int kVec = kBf16 ? 8 : 16;
+  if (vec_ok && c1 - c0 == kTileN) {
+    // The tile's rows as 16-byte chunks; consecutive threads take consecutive
+    // chunks of a row, so a warp reads whole rows (coalesced), and every load
+    // of a thread is independent of the others.
+    constexpr int kVec = kBf16 ? kTileN * 2 / 16 : kTileN * 4 / 16;  // chunks per row
+#pragma unroll
+    for (int t = 0; t < kVec; ++t) {
+      const int c = t * kScanThreads + (int)threadIdx.x;
+      const int row = r0 + c / kVec;
+      if (row >= Q) continue;
       const uint4* p = reinterpret_cast<const uint4*>(static_cast<const char*>(mask) +
-                                                      (base + c0) * (kBf16 ? 2 : 4));
+                                                      (((size_t)b * Q + row) * (size_t)K + c0) * (kBf16 ? 2 : 4)) +
+                       (c % kVec);
+      const uint4 w = __ldg(p);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int t = 0; t < kVec; ++t) {
-        const uint4 w = __ldg(p + t);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          bool z0, n0;
-          if (kBf16) {
-            bool z1, n1;
-            classify_bits(ws[u] & 0xFFFFu, true, z0, n0);
-            classify_bits(ws[u] >> 16, true, z1, n1);
-            all_zero &= z0 && z1;
-            all_ninf &= n0 && n1;
-          } else {
-            classify_bits(ws[u], false, z0, n0);
-            all_zero &= z0;
-            all_ninf &= n0;
-          }
+      for (int u = 0; u < 4; ++u) {
+        bool z0, n0;
+        if (kBf16) {
+          bool z1, n1;
+          classify_bits(ws[u] & 0xFFFFu, true, z0, n0);
+          classify_bits(ws[u] >> 16, true, z1, n1);
+          all_zero &= z0 && z1;
+          all_ninf &= n0 && n1;
+        } else {
+          classify_bits(ws[u], false, z0, n0);
+          all_zero &= z0;
+          all_ninf &= n0;
         }
       }
-    } else {
+    }
+  } else {
+    // ragged tile or unaligned rows: element by element, a row per thread
+    const int row = r0 + (int)threadIdx.x;
+    if (row < Q) {
+      const size_t base = ((size_t)b * Q + row) * (size_t)K;
       for (int c = c0; c < c1; ++c) {
         uint32_t bits = kBf16 ? (uint32_t) static_cast<const uint16_t*>(mask)[base + c]
                               : static_cast<const uint32_t*>(mask)[base + c];

@@ -317,6 +317,12 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
                : "memory");
 }
 
+// Brings the cache line holding `p` into L1 (no register result, no fault on
+// any address the kernel may read).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Three-input maximum (sm_100 and later).
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
