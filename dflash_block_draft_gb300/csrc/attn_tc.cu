@@ -23,10 +23,13 @@
 // registers a thread: 128*120 + 256*192 = 384*168, the launch budget.  Each
 // half's MMAs go out from its own thread in the order
 //   QK_i(j) [softmax_i(j)] PV_i(j) QK_i(j+1) ...
-// (PV_i(j) and QK_i(j+1) back to back once P_i(j) is there).  Left free, the
-// two issue streams interleave in the tensor pipe and the halves run in step;
-// making them take turns would let one half's softmax overlap the other half's
-// MMAs, but then the ring must hold two key tiles per half, more than fits.
+// PV_i(j) goes out in two parts: keys 0-63 as soon as the softmax has written
+// that half of P (so it runs during the softmax of keys 64-127), then keys
+// 64-127 and QK_i(j+1) back to back.  Left free, the two issue streams
+// interleave in the tensor pipe and the halves run in step; making them take
+// turns would let one half's softmax overlap the other half's MMAs, but then
+// the ring must hold two key tiles per half, more than fits (the CTA-pair
+// kernel of attn_tc2.cu does that).
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
 // P_i (bf16 pairs) overwrites the first 64 columns of S_i once they are read,
 // and QK_i(j+1) is issued only after PV_i(j), which the tensor pipe runs in order.
@@ -66,8 +69,10 @@ enum {
   BAR_RING_FULL = 2,                       // kRing
   BAR_RING_EMPTY = BAR_RING_FULL + kRing,  // kRing
   BAR_S_FULL = BAR_RING_EMPTY + kRing,     // 2 (per half)
-  BAR_P_FULL = BAR_S_FULL + 2,             // 2
-  BAR_O_FULL = BAR_P_FULL + 2,             // 2
+  BAR_P_LO = BAR_S_FULL + 2,               // 2: P of keys 0-63 written
+  BAR_P_HI = BAR_P_LO + 2,                 // 2: P of keys 64-127 written
+  BAR_PV_LO = BAR_P_HI + 2,                // 2: PV of keys 0-63 completed
+  BAR_O_FULL = BAR_PV_LO + 2,              // 2
   BAR_DRAIN = BAR_O_FULL + 2,
   kNumBars = BAR_DRAIN + 1
 };
@@ -235,7 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ctl.bar(BAR_S_FULL + i), 1);
-      ptx::mbar_init(ctl.bar(BAR_P_FULL + i), 128);
+      ptx::mbar_init(ctl.bar(BAR_P_LO + i), 128);
+      ptx::mbar_init(ctl.bar(BAR_P_HI + i), 128);
+      ptx::mbar_init(ctl.bar(BAR_PV_LO + i), 1);
       ptx::mbar_init(ctl.bar(BAR_O_FULL + i), 1);
     }
     ptx::mbar_init(ctl.bar(BAR_DRAIN), 2);  // both MMA issuers
@@ -331,10 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_commit(ctl.bar(BAR_S_FULL + i));
       };
-      auto issue_pv = [&](uint32_t gg, bool first) {
+      auto issue_pv = [&](uint32_t gg, bool first, int ks0) {
         const uint64_t dv = dRingV + (((v_panel0(gg) % kRing) * kPanel) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
+        for (int ks = ks0; ks < ks0 + kBN / 32; ++ks) {
           // 16 keys: 8 packed P columns; V rows: two 1024-byte groups of 8 keys;
           // the 128 output columns span both V panels (LBO = one panel)
           ptx::mma_ts(d_o, d_s + (uint32_t)ks * 8u, dv + (((uint32_t)ks * 2048u) >> 4), kIdescPV,
@@ -345,13 +352,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // before P_i, so that the MMAs go out right after P_i arrives).
       auto pv_ready = [&](uint32_t gg) -> bool {
         const uint32_t vp = v_panel0(gg);
-        return panel_ready(vp) && panel_ready(vp + 1) && ctl.wait(BAR_P_FULL + i, gg & 1u);
+        return panel_ready(vp) && panel_ready(vp + 1) && ctl.wait(BAR_P_LO + i, gg & 1u);
       };
-      auto pv_issue = [&](uint32_t gg, bool first) {
+      // PV of keys 0-63, then (once the softmax has written it) of keys 64-127.
+      auto pv_issue = [&](uint32_t gg, bool first) -> bool {
         const uint32_t vp = v_panel0(gg);
-        issue_pv(gg, first);
+        issue_pv(gg, first, 0);
+        ptx::tc_commit(ctl.bar(BAR_PV_LO + i));
+        if (!ctl.wait(BAR_P_HI + i, gg & 1u)) return false;
+        ptx::tc_fence_after();
+        issue_pv(gg, false, kBN / 32);
         release(vp);
         release(vp + 1);
+        return true;
       };
       bool stop = false;
       for (int k = 0; !stop && k * (int)gridDim.x < a.n_items; ++k) {
@@ -378,7 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::tc_fence_after();
           if (!first_tile) {
-            pv_issue(g - 1, first_pv);
+            if (!pv_issue(g - 1, first_pv)) {
+              stop = true;
+              break;
+            }
             first_pv = false;
           }
           issue_qk(g);
@@ -394,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));  // every QK of this half has been issued
         if (!pv_ready(g - 1)) break;  // PV of the item's last tile
         ptx::tc_fence_after();
-        pv_issue(g - 1, first_pv);
+        if (!pv_issue(g - 1, first_pv)) break;
         ptx::tc_commit(ctl.bar(BAR_O_FULL + i));
       }
       // Drain: every MMA this thread issued has finished before TMEM is released.
@@ -475,9 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // low half) over the first 64 columns of S, which are already read.  Only
         // when a half's maximum exceeds m by more than 2^8 -- always on the row's
         // first visible scores, rarely afterwards -- does m move; everything built
-        // with the old m is then scaled by alpha = exp2(m_old - m_new): O (PV of
-        // the previous tile has completed: it was issued before this tile's QK),
-        // l, and the P columns this tile already wrote.
+        // with the old m is then scaled by alpha = exp2(m_old - m_new): O and l.
+        // P of keys 0-63 is handed to the MMA issuer as soon as it is written, so
+        // that PV of those keys runs while the second half is computed; a rescale
+        // in the second half therefore waits for that PV and scales O after it.
+        // (At the first half, PV of the previous tile has completed: it was
+        // issued before this tile's QK.)
         const bool scaled = kind == kPrepDense;  // dense scores are already in base-2 units
         const float cm = scaled ? 1.f : c2;
         float2 lsum = make_float2(0.f, 0.f);
@@ -492,6 +511,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (mh > m_used + 8.0f) {  // also when m is still -inf and this half sees a key
             if (m_used != -INFINITY) {
               const float alpha = ptx::ex2(m_used - mh);
+              // the second half: O may still be taking PV of keys 0-63 (P written
+              // with the old reference); scale O once that has completed
+              if (hh == 1 && !ctl.wait(BAR_PV_LO + half, g & 1u)) stop = true;
+              ptx::tc_fence_after();
 #pragma unroll 1
               for (int cc = 0; cc < kDv; cc += 32) {
                 uint32_t o[32];
@@ -500,17 +523,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                 ptx::tmem_st32(o_col + cc, o);
-              }
-              if (hh == 1) {  // P of columns 0-63, written with the old reference
-                uint32_t pr[32];
-                ptx::tmem_wait_st();
-                ptx::tmem_ld32(s_col, pr);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  pr[e] = ptx::pack_bf16x2(__uint_as_float(pr[e] << 16) * alpha,
-                                           __uint_as_float(pr[e] & 0xFFFF0000u) * alpha);
-                ptx::tmem_st32(s_col, pr);
               }
               ptx::tmem_wait_st();
               l *= alpha;
@@ -530,11 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[c / 2] = ptx::pack_bf16x2(pp.x, pp.y);
           }
           ptx::tmem_st32(s_col + 32u * hh, pk);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(ctl.bar((hh == 0 ? BAR_P_LO : BAR_P_HI) + half));
         }
+        if (stop) break;
         l += lsum.x + lsum.y;
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(ctl.bar(BAR_P_FULL + half));
         ++g;
       }
       if (stop) break;
