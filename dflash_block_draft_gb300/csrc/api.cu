@@ -158,17 +158,17 @@ bool use_tc(dflash_dtype_t dtype, int dn, int dr, int dv, long long q_rows, long
 
 // Two tensor-core kernels compute the same result.  attn_tc2.cu (CTA pairs,
 // items of four query tiles) alternates the two halves of an item on the
-// tensor pipe and wins on long contexts; attn_tc.cu (one CTA, items of two
-// query tiles) has less masked work per item and finer load balance, and wins
-// on short ones.  The switch is at 16384 keys per segment on average (measured
-// on GB300, anchored: S+Q = 8192 favours attn_tc.cu by 13 %, 16384 is even,
-// 34816 favours the pair kernel by 10 %).  Dense masks stay on attn_tc.cu: the
-// pair kernel's per-tile class lookups over four query tiles cost it 10-25 %.
-// DFLASH_TC_KERNEL=1 or 2 forces one.
+// tensor pipe and wins on very long contexts; attn_tc.cu (one CTA, items of
+// two query tiles) has less masked work per item and finer load balance, and
+// wins on shorter ones.  The switch is at 32768 keys per segment on average
+// (measured on GB300, anchored: S+Q = 8192 and 16384 favour attn_tc.cu by 13 %
+// and 7 %, 34816 favours the pair kernel by 1 %).  Dense masks stay on
+// attn_tc.cu: the pair kernel's per-tile class lookups over four query tiles
+// cost it 10-25 %.  DFLASH_TC_KERNEL=1 or 2 forces one.
 cudaError_t launch_tc(const AttnParams& p, int segments, int nqt, long long q_rows, long long kv_rows,
                       cudaStream_t stream) {
   const char* force = getenv("DFLASH_TC_KERNEL");
-  bool pair = p.mode != kDense && segments > 0 && kv_rows / segments >= 16384;
+  bool pair = p.mode != kDense && segments > 0 && kv_rows / segments >= 32768;
   if (force && force[0] == '1') pair = false;
   if (force && force[0] == '2') pair = true;
   if (pair) return launch_attn_tc2(p, segments, nqt, q_rows, kv_rows, stream);
