@@ -96,6 +96,7 @@ struct Tc2Args {
   int nquad;    // ceil(nqt / 4)
   int n_items;  // nquad * segments * H
   int mask_vec; // dense: mask rows are 16-byte aligned
+  int out_v8;   // out is 32-byte aligned: rows are written with 32-byte stores
 };
 
 struct Item {
@@ -579,8 +580,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (row_ok) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
                                               ((it.sg.q0 + i) * p.H + it.h) * (long long)kDv);
+        if (a.out_v8) {
+          // a row is 256 contiguous bytes: eight 32-byte stores (a sector each)
 #pragma unroll
-        for (int v = 0; v < kDv / 8; ++v) dst[v] = make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]);
+          for (int v = 0; v < kDv / 16; ++v) ptx::st_global_v8(dst + 2 * v, ob + 8 * v);
+        } else {
+#pragma unroll
+          for (int v = 0; v < kDv / 8; ++v) dst[v] = make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]);
+        }
         if (p.lse)
           p.lse[it.sg.lse0 + (long long)it.h * it.sg.lse_hs + i] =
               l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
@@ -609,6 +616,7 @@ cudaError_t launch_attn_tc2(const AttnParams& p, int segments, int nqt, long lon
   a.n_items = a.nquad * segments * p.H;
   a.mask_vec = 0;
   if (p.mode == kDense) a.mask_vec = (((uintptr_t)p.mask & 15u) == 0) && ((p.S + p.Q) % 8 == 0);
+  a.out_v8 = ((uintptr_t)p.out & 31u) == 0;
   if (a.n_items <= 0) return cudaSuccess;
   CUtensorMap mq, mkn, mkr, mv;
   if (!make_map_3d(&mq, p.q, q_rows, p.H, kDn + kDr, kBM) || !make_map_3d(&mkn, p.kn, kv_rows, p.H, kDn, kBN / 2) ||

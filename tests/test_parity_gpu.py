@@ -125,6 +125,25 @@ def test_dense_general_mask_with_finite_values_and_empty_rows(dfl):
     assert np.all(got_o[1, 7] == 0) and np.all(np.isneginf(got_l[1, :, 7]))
 
 
+@pytest.mark.parametrize("tc", ["1", "2"])
+def test_output_only_16_byte_aligned(dfl, tc, monkeypatch):
+    """The tensor-core kernels write rows with 32-byte stores when `out` is 32-byte
+    aligned and with 16-byte stores otherwise; both give the same bytes."""
+    monkeypatch.setenv("DFLASH_TC_KERNEL", tc)
+    d = _small_case("bf16", 1, 2, 1024, 40, 16, 128, 64, 128)
+    t = _dev(d, "bf16")
+    an = torch.from_numpy(d["anchors"]).cuda()
+    B, Q, H, dv = d["B"], d["Q"], d["H"], d["d_v"]
+    ref = dfl.dflash_attn_anchored(t["q"], t["k_nope"], t["k_rope"], t["v"], an, d["block_size"])
+    flat = torch.full((B * Q * H * dv + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = flat[8:].view(B, Q, H, dv)  # 16 bytes past a 32-byte boundary
+    assert out.data_ptr() % 32 == 16
+    dfl.dflash_attn_anchored(t["q"], t["k_nope"], t["k_rope"], t["v"], an, d["block_size"], out=out)
+    assert dfl.dflash_last_device_error() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.isnan(flat[:8]).all()  # nothing written before the output
+
+
 def test_single_visible_key_returns_value_row_exactly(dfl, kernel):
     d = _small_case("bf16", 1, 2, 200, 20, 8, 128, 64, 128, seed=9)
     Q, K = d["Q"], d["S"] + d["Q"]
