@@ -25,11 +25,13 @@
 //   QK_i(j) [softmax_i(j)] PV_i(j) QK_i(j+1) ...
 // PV_i(j) goes out in two parts: keys 0-63 as soon as the softmax has written
 // that half of P (so it runs during the softmax of keys 64-127), then keys
-// 64-127 and QK_i(j+1) back to back.  Left free, the two issue streams
-// interleave in the tensor pipe and the halves run in step; making them take
-// turns would let one half's softmax overlap the other half's MMAs, but then
-// the ring must hold two key tiles per half, more than fits (the CTA-pair
-// kernel of attn_tc2.cu does that).
+// 64-127 and QK_i(j+1) back to back.  The QKs of the two halves take turns
+// (QK_0(j), QK_1(j), QK_0(j+1), ...), so S_1 lands one QK after S_0 and the
+// two softmax warpgroups run staggered rather than in step; left free, the
+// two issue streams interleave MMA by MMA and both S land together.  Turns on
+// whole groups (PV and QK) would let one half's softmax overlap all of the
+// other half's MMAs, but then the ring must hold two key tiles per half, more
+// than fits (the CTA-pair kernel of attn_tc2.cu does that).
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
 // P_i (bf16 pairs) overwrites the first 64 columns of S_i once they are read,
 // and QK_i(j+1) is issued only after PV_i(j), which the tensor pipe runs in order.
@@ -72,7 +74,8 @@ enum {
   BAR_P_LO = BAR_S_FULL + 2,               // 2: P of keys 0-63 written
   BAR_P_HI = BAR_P_LO + 2,                 // 2: P of keys 64-127 written
   BAR_PV_LO = BAR_P_HI + 2,                // 2: PV of keys 0-63 completed
-  BAR_O_FULL = BAR_PV_LO + 2,              // 2
+  BAR_QK_TURN = BAR_PV_LO + 2,             // 2: QK_i(g) issued
+  BAR_O_FULL = BAR_QK_TURN + 2,            // 2
   BAR_DRAIN = BAR_O_FULL + 2,
   kNumBars = BAR_DRAIN + 1
 };
@@ -244,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ctl.bar(BAR_P_LO + i), 128);
       ptx::mbar_init(ctl.bar(BAR_P_HI + i), 128);
       ptx::mbar_init(ctl.bar(BAR_PV_LO + i), 1);
+      ptx::mbar_init(ctl.bar(BAR_QK_TURN + i), 1);
       ptx::mbar_init(ctl.bar(BAR_O_FULL + i), 1);
     }
     ptx::mbar_init(ctl.bar(BAR_DRAIN), 2);  // both MMA issuers
@@ -398,7 +402,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             first_pv = false;
           }
+          // QK of half 1 after QK of half 0 of the same tile, QK of half 0 after QK of
+          // half 1 of the previous tile: S_1 lands one QK after S_0, so the two
+          // softmax warpgroups start apart instead of together.
+          if (i == 1 ? !ctl.wait(BAR_QK_TURN + 0, g & 1u) : (g > 0 && !ctl.wait(BAR_QK_TURN + 1, (g - 1) & 1u))) {
+            stop = true;
+            break;
+          }
           issue_qk(g);
+          ptx::mbar_arrive(ctl.bar(BAR_QK_TURN + i));
           release(kp);
           release(kp + 1);
           release(kp + 2);
