@@ -134,6 +134,8 @@ struct Item {
   int ctx_end, noise_begin, noise_end;  // anchored: the pair's non-SKIP tiles are [0,ctx_end) U [noise_begin,noise_end)
 };
 
+// DENSE: the kernel reads tile classes of a dense mask (else the anchored rule).
+template <bool DENSE>
 __device__ __forceinline__ Item decode_item(const TcArgs& a, int idx) {
   Item it;
   const AttnParams& p = a.p;
@@ -157,7 +159,7 @@ __device__ __forceinline__ Item decode_item(const TcArgs& a, int idx) {
     it.amin[i] = S;
     it.amax[i] = 0;
     if (!it.has[i]) continue;
-    if (p.mode == kDense) {
+    if (DENSE) {
       it.cls[i] = p.classes + ((long long)it.z * p.nqt + t) * p.nkt;
     } else {
       // The tile's anchors, eight independent loads at a time (a load-use chain
@@ -178,7 +180,7 @@ __device__ __forceinline__ Item decode_item(const TcArgs& a, int idx) {
     }
   }
   it.ok = it.has[0];
-  if (it.ok && p.mode != kDense) {
+  if (it.ok && !DENSE) {
     // Context keys some row sees: k < max anchor.  Noise keys some row sees: the
     // blocks of the pair's rows, [blk(first row) * bs, (blk(last row) + 1) * bs) within Q.
     const int amax = max(it.amax[0], it.has[1] ? it.amax[1] : 0);
@@ -193,9 +195,10 @@ __device__ __forceinline__ Item decode_item(const TcArgs& a, int idx) {
 }
 
 // Next key tile after kt that either half needs (it.nkt when none is left).
+template <bool DENSE>
 __device__ __forceinline__ int next_tile(const TcArgs& a, const Item& it, int kt) {
   ++kt;
-  if (a.p.mode != kDense) {
+  if (!DENSE) {
     if (kt < it.ctx_end) return kt;
     kt = max(kt, it.noise_begin);
     return kt < it.noise_end ? kt : it.nkt;
@@ -206,10 +209,11 @@ __device__ __forceinline__ int next_tile(const TcArgs& a, const Item& it, int kt
 }
 
 // Class of tile kt for the query tile of one half, from that half's scalars.
+template <bool DENSE>
 __device__ __forceinline__ int half_class(const TcArgs& a, const Seg& sg, bool has, int r0, int r1, int amin,
                                           int amax, const uint8_t* cls, int kt) {
   if (!has) return DFLASH_TILE_SKIP;
-  if (a.p.mode == kDense) return cls[kt];
+  if (DENSE) return cls[kt];
   return anchored_tile_class(sg.S, sg.Q, a.p.bs, r0, r1, amin, amax, kt);
 }
 
@@ -219,6 +223,7 @@ __device__ __forceinline__ int item_of_round(int k) {
   return k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
 }
 
+template <bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmKn, const __grid_constant__ CUtensorMap tmKr,
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; !stop && k * (int)gridDim.x < a.n_items; ++k) {
         const int idx = item_of_round(k);
         if (idx >= a.n_items) continue;
-        const Item it = decode_item(a, idx);
+        const Item it = decode_item<DENSE>(a, idx);
         if (!it.ok) continue;
         if (n_items > 0 && !ctl.wait(BAR_Q_EMPTY, (n_items - 1) & 1u)) break;
         ptx::mbar_arrive_expect_tx(ctl.bar(BAR_Q_FULL), 2 * kQBytes);
@@ -291,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              qrow);
         }
         ++n_items;
-        for (int kt = next_tile(a, it, -1); kt < it.nkt && !stop; kt = next_tile(a, it, kt)) {
+        for (int kt = next_tile<DENSE>(a, it, -1); kt < it.nkt && !stop; kt = next_tile<DENSE>(a, it, kt)) {
           const int krow = (int)(it.sg.kv0 + (long long)kt * kBN);
           const bool vf = v_first(pc / kPanelsPerTile);
           for (uint32_t pn = 0; pn < kPanelsPerTile; ++pn, ++pc) {
@@ -375,18 +380,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; !stop && k * (int)gridDim.x < a.n_items; ++k) {
         const int idx = item_of_round(k);
         if (idx >= a.n_items) continue;
-        const Item it = decode_item(a, idx);
+        const Item it = decode_item<DENSE>(a, idx);
         if (!it.ok) continue;
         if (!ctl.wait(BAR_Q_FULL, n_items & 1u)) break;
         ++n_items;
-        int kt = next_tile(a, it, -1);
+        int kt = next_tile<DENSE>(a, it, -1);
         if (kt >= it.nkt) {  // nothing visible for this pair of query tiles
           ptx::tc_commit(ctl.bar(BAR_Q_EMPTY));
           continue;
         }
         bool first_tile = true, first_pv = true;
         for (;;) {
-          const int kn = next_tile(a, it, kt);
+          const int kn = next_tile<DENSE>(a, it, kt);
           const uint32_t kp = k_panel0(g);  // first K panel of tile g
           // The K panels never wait on this half's PV of tile g-1: the ring slots they
           // reuse were freed by MMAs of tiles g-2 and earlier, or by QK of tile g-1.
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; !stop && k * (int)gridDim.x < a.n_items; ++k) {
       const int idx = item_of_round(k);
       if (idx >= a.n_items) continue;
-      const Item it = decode_item(a, idx);
+      const Item it = decode_item<DENSE>(a, idx);
       if (!it.ok) continue;
       // this half's scalars (selected, so that the item's arrays stay in registers)
       const bool h_has = half ? it.has[1] : it.has[0];
@@ -463,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int S = it.sg.S, Qn = it.sg.Q, K = S + Qn;
       int ctx_lim = 0, nlo = 0, nhi = 0;
       const __nv_bfloat16* mrow = nullptr;
-      if (p.mode == kDense) {
+      if (DENSE) {
         mrow = static_cast<const __nv_bfloat16*>(p.mask) + ((long long)it.z * p.Q + (row_ok ? i : 0)) * (long long)K;
       } else if (row_ok) {
         ctx_lim = row_anchor(p, it.sg, i);
@@ -473,9 +478,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float m_used = -INFINITY, l = 0.f;
       bool any_tile = false;
-      for (int kt = next_tile(a, it, -1); kt < it.nkt; kt = next_tile(a, it, kt)) {
+      int kt = next_tile<DENSE>(a, it, -1);
+      int cls = kt < it.nkt ? half_class<DENSE>(a, it.sg, h_has, h_r0, h_r1, h_amin, h_amax, h_cls, kt) : 0;
+      while (kt < it.nkt) {
         any_tile = true;
-        const int cls = half_class(a, it.sg, h_has, h_r0, h_r1, h_amin, h_amax, h_cls, kt);
+        // With a dense mask the next tile and its class are loads of tile-class
+        // bytes: they are looked up before the wait for this tile's scores, so that
+        // their latency overlaps the wait instead of following this tile (the
+        // anchored schedule is arithmetic and is evaluated after the tile).
+        int kn = 0, cls_n = 0;
+        if (DENSE) {
+          kn = next_tile<DENSE>(a, it, kt);
+          cls_n = kn < it.nkt ? half_class<DENSE>(a, it.sg, h_has, h_r0, h_r1, h_amin, h_amax, h_cls, kn) : 0;
+        }
         const int k0 = kt * kBN;
         // How this row treats the tile: plain scores, anchored mask, dense mask, or
         // nothing.  A FULL tile that runs past the segment's last key still needs the
@@ -483,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kind;
         if (!row_ok || cls == DFLASH_TILE_SKIP) kind = kPrepNone;
         else if (cls == DFLASH_TILE_FULL && k0 + kBN <= K) kind = kPrepFull;
-        else kind = p.mode == kDense ? kPrepDense : kPrepAnchored;
+        else kind = DENSE ? kPrepDense : kPrepAnchored;
         const PrepCtx pc{ctx_lim - k0, nlo - k0, nhi - k0, mrow ? mrow + k0 : nullptr, K - k0,
                          a.mask_vec != 0, c2};
         if (kind == kPrepDense) {
@@ -562,6 +577,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (stop) break;
         l += lsum.x + lsum.y;
         ++g;
+        if (!DENSE) {
+          kn = next_tile<DENSE>(a, it, kt);
+          cls_n = kn < it.nkt ? half_class<DENSE>(a, it.sg, h_has, h_r0, h_r1, h_amin, h_amax, h_cls, kn) : 0;
+        }
+        kt = kn;
+        cls = cls_n;
       }
       if (stop) break;
       // ---- epilogue: out = O / l (bf16, round to nearest even), lse = (m + log2 l) ln 2
@@ -683,13 +704,14 @@ cudaError_t launch_attn_tc(const AttnParams& p, int segments, int nqt, long long
   if (nsm <= 0) return cudaErrorInvalidDevice;
   // The setmaxnreg split assumes the kernel launches with exactly kLaunchRegs
   // registers per thread; any other count would make setmaxnreg.inc wait forever.
+  auto kernel = p.mode == kDense ? attn_tc_kernel<true> : attn_tc_kernel<false>;
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, attn_tc_kernel) != cudaSuccess || fa.numRegs != kLaunchRegs)
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess || fa.numRegs != kLaunchRegs)
     return cudaErrorInvalidConfiguration;
   const int grid = a.n_items < nsm ? a.n_items : nsm;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, mq, mkn, mkr, mv);
+  kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, mq, mkn, mkr, mv);
   count_launch();
   return cudaGetLastError();
 }
