@@ -156,19 +156,18 @@ bool use_tc(dflash_dtype_t dtype, int dn, int dr, int dv, long long q_rows, long
   return !env_flag("DFLASH_FORCE_SIMT");
 }
 
-// Two tensor-core kernels compute the same result.  attn_tc2.cu (CTA pairs,
-// items of four query tiles) alternates the two halves of an item on the
-// tensor pipe and wins on very long contexts; attn_tc.cu (one CTA, items of
-// two query tiles) has less masked work per item and finer load balance, and
-// wins on shorter ones.  The switch is at 32768 keys per segment on average
-// (measured on GB300, anchored: S+Q = 8192 and 16384 favour attn_tc.cu by 13 %
-// and 7 %, 34816 favours the pair kernel by 1 %).  Dense masks stay on
-// attn_tc.cu: the pair kernel's per-tile class lookups over four query tiles
-// cost it 10-25 %.  DFLASH_TC_KERNEL=1 or 2 forces one.
+// Two tensor-core kernels compute the same result.  attn_tc.cu (one CTA per
+// item of two query tiles) is the default: measured on GB300 it is the faster
+// of the two on every bf16 workload (anchored, S+Q = 8192 / 16384 / 34816:
+// by 13 %, 10 % and 5 %; dense by more).  attn_tc2.cu (CTA pairs, items of
+// four query tiles, tcgen05 pair MMAs) alternates the two halves of an item on
+// the tensor pipe, but its pair QK runs at about half the per-SM MMA rate and
+// its larger items carry more masked work.  DFLASH_TC_KERNEL=2 selects it
+// (DFLASH_TC_KERNEL=1 the default kernel).
 cudaError_t launch_tc(const AttnParams& p, int segments, int nqt, long long q_rows, long long kv_rows,
                       cudaStream_t stream) {
   const char* force = getenv("DFLASH_TC_KERNEL");
-  bool pair = p.mode != kDense && segments > 0 && kv_rows / segments >= 32768;
+  bool pair = false;
   if (force && force[0] == '1') pair = false;
   if (force && force[0] == '2') pair = true;
   if (pair) return launch_attn_tc2(p, segments, nqt, q_rows, kv_rows, stream);

@@ -130,6 +130,8 @@ __device__ __forceinline__ void anchor_range(const AttnParams& p, const Seg& sg,
   }
 }
 
+// DENSE: the kernel reads tile classes of a dense mask (else the anchored rule).
+template <bool DENSE>
 __device__ __forceinline__ Item decode_item(const Tc2Args& a, int idx, uint32_t rank) {
   Item it;
   const AttnParams& p = a.p;
@@ -153,14 +155,14 @@ __device__ __forceinline__ Item decode_item(const Tc2Args& a, int idx, uint32_t 
     it.amin[i] = S;
     it.amax[i] = 0;
     if (!it.has[i]) continue;
-    if (p.mode == kDense) it.cls[i] = p.classes + ((long long)it.z * p.nqt + t) * p.nkt;
+    if (DENSE) it.cls[i] = p.classes + ((long long)it.z * p.nqt + t) * p.nkt;
     else anchor_range(p, it.sg, it.r0[i], it.r1[i], it.amin[i], it.amax[i]);
   }
   const int q_first = 4 * quad * kBM;
   it.ok = q_first < Qn;
   if (!it.ok) return it;
   const int q_last = min(q_first + 4 * kBM, Qn);  // rows [q_first, q_last) of the item
-  if (p.mode == kDense) {
+  if (DENSE) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int t = 4 * quad + j;
@@ -181,9 +183,10 @@ __device__ __forceinline__ Item decode_item(const Tc2Args& a, int idx, uint32_t 
 }
 
 // Next key tile after kt that some row of the item needs (it.nkt when none is left).
+template <bool DENSE>
 __device__ __forceinline__ int next_tile(const Tc2Args& a, const Item& it, int kt) {
   ++kt;
-  if (a.p.mode != kDense) {
+  if (!DENSE) {
     if (kt < it.ctx_end) return kt;
     kt = max(kt, it.noise_begin);
     return kt < it.noise_end ? kt : it.nkt;
@@ -196,10 +199,11 @@ __device__ __forceinline__ int next_tile(const Tc2Args& a, const Item& it, int k
   return it.nkt;
 }
 
+template <bool DENSE>
 __device__ __forceinline__ int half_class(const Tc2Args& a, const Seg& sg, bool has, int r0, int r1, int amin,
                                           int amax, const uint8_t* cls, int kt) {
   if (!has) return DFLASH_TILE_SKIP;
-  if (a.p.mode == kDense) return cls[kt];
+  if (DENSE) return cls[kt];
   return anchored_tile_class(sg.S, sg.Q, a.p.bs, r0, r1, amin, amax, kt);
 }
 
@@ -209,6 +213,7 @@ __device__ __forceinline__ int item_of_round(int k) {
   return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
+template <bool DENSE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_tc2_kernel(const __grid_constant__ Tc2Args a, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmKn, const __grid_constant__ CUtensorMap tmKr,
@@ -275,7 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int k = 0; !stop && k * G < a.n_items; ++k) {
         const int idx = item_of_round(k);
         if (idx >= a.n_items) continue;
-        const Item it = decode_item(a, idx, rank);
+        const Item it = decode_item<DENSE>(a, idx, rank);
         if (!it.ok) continue;
         if (n_items > 0 && !ctl.wait_cluster(BAR_Q_EMPTY, (n_items - 1) & 1u)) break;
         ptx::mbar_arrive_expect_tx(ctl.bar(BAR_Q_FULL), 2 * kQBytes);
@@ -286,7 +291,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              qrow);
         }
         ++n_items;
-        for (int kt = next_tile(a, it, -1); kt < it.nkt; kt = next_tile(a, it, kt), ++g) {
+        for (int kt = next_tile<DENSE>(a, it, -1); kt < it.nkt; kt = next_tile<DENSE>(a, it, kt), ++g) {
           const uint32_t s = g % kSlots;
           if (!ctl.wait_cluster(BAR_EMPTY + s, ((g / kSlots) & 1u) ^ 1u)) {
             stop = true;
@@ -317,12 +322,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int k = 0; !stop && k * G < a.n_items; ++k) {
         const int idx = item_of_round(k);
         if (idx >= a.n_items) continue;
-        const Item it = decode_item(a, idx, rank);
+        const Item it = decode_item<DENSE>(a, idx, rank);
         if (!it.ok) continue;
         if (!ctl.wait_cluster(BAR_Q_FULL, n_items & 1u)) break;
         forward(BAR_Q_FULL);
         ++n_items;
-        for (int kt = next_tile(a, it, -1); kt < it.nkt; kt = next_tile(a, it, kt), ++g) {
+        for (int kt = next_tile<DENSE>(a, it, -1); kt < it.nkt; kt = next_tile<DENSE>(a, it, kt), ++g) {
           const uint32_t s = g % kSlots, ph = (g / kSlots) & 1u;
           if (!ctl.wait_cluster(BAR_K_FULL + s, ph)) {
             stop = true;
@@ -387,18 +392,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int k = 0; !stop && k * G < a.n_items; ++k) {
         const int idx = item_of_round(k);
         if (idx >= a.n_items) continue;
-        const Item it = decode_item(a, idx, rank);
+        const Item it = decode_item<DENSE>(a, idx, rank);
         if (!it.ok) continue;
         if (!ctl.wait_cluster(BAR_Q_FULL, n_items & 1u)) break;
         ++n_items;
-        int kt = next_tile(a, it, -1);
+        int kt = next_tile<DENSE>(a, it, -1);
         if (kt >= it.nkt) {  // nothing visible for this item
           ptx::tc_commit_pair(ctl.bar(BAR_Q_EMPTY));
           continue;
         }
         bool first_tile = true, first_pv = true;
         for (;;) {
-          const int kn = next_tile(a, it, kt);
+          const int kn = next_tile<DENSE>(a, it, kt);
           if (!ctl.wait_cluster(BAR_K_FULL + g % kSlots, (g / kSlots) & 1u) || (!first_tile && !pv_ready(g - 1)) ||
               !take_turn()) {
             stop = true;
@@ -451,7 +456,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int k = 0; !stop && k * G < a.n_items; ++k) {
       const int idx = item_of_round(k);
       if (idx >= a.n_items) continue;
-      const Item it = decode_item(a, idx, rank);
+      const Item it = decode_item<DENSE>(a, idx, rank);
       if (!it.ok) continue;
       // this half's scalars (selected, so that the item's arrays stay in registers)
       const bool h_has = half ? it.has[1] : it.has[0];
@@ -463,7 +468,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int S = it.sg.S, Qn = it.sg.Q, K = S + Qn;
       int ctx_lim = 0, nlo = 0, nhi = 0;
       const __nv_bfloat16* mrow = nullptr;
-      if (p.mode == kDense) {
+      if (DENSE) {
         mrow = static_cast<const __nv_bfloat16*>(p.mask) + ((long long)it.z * p.Q + (row_ok ? i : 0)) * (long long)K;
       } else if (row_ok) {
         ctx_lim = row_anchor(p, it.sg, i);
@@ -473,14 +478,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       float m_used = -INFINITY, l = 0.f;
       bool any_tile = false;
-      for (int kt = next_tile(a, it, -1); kt < it.nkt; kt = next_tile(a, it, kt)) {
+      for (int kt = next_tile<DENSE>(a, it, -1); kt < it.nkt; kt = next_tile<DENSE>(a, it, kt)) {
         any_tile = true;
-        const int cls = half_class(a, it.sg, h_has, h_r0, h_r1, h_amin, h_amax, h_cls, kt);
+        const int cls = half_class<DENSE>(a, it.sg, h_has, h_r0, h_r1, h_amin, h_amax, h_cls, kt);
         const int k0 = kt * kBN;
         int kind;
         if (!row_ok || cls == DFLASH_TILE_SKIP) kind = kPrepNone;
         else if (cls == DFLASH_TILE_FULL && k0 + kBN <= K) kind = kPrepFull;
-        else kind = p.mode == kDense ? kPrepDense : kPrepAnchored;
+        else kind = DENSE ? kPrepDense : kPrepAnchored;
         const PrepCtx pc{ctx_lim - k0, nlo - k0, nhi - k0, mrow ? mrow + k0 : nullptr, K - k0,
                          a.mask_vec != 0, c2};
         if (!ctl.wait_cluster(BAR_S_FULL + half, g & 1u)) {
@@ -626,13 +631,14 @@ cudaError_t launch_attn_tc2(const AttnParams& p, int segments, int nqt, long lon
   if (nsm < 2) return cudaErrorInvalidDevice;
   // The setmaxnreg split assumes the kernel launches with exactly kLaunchRegs
   // registers per thread; any other count would make setmaxnreg.inc wait forever.
+  auto kernel = p.mode == kDense ? attn_tc2_kernel<true> : attn_tc2_kernel<false>;
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, attn_tc2_kernel) != cudaSuccess || fa.numRegs != kLaunchRegs)
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess || fa.numRegs != kLaunchRegs)
     return cudaErrorInvalidConfiguration;
   const int clusters = a.n_items < nsm / 2 ? a.n_items : nsm / 2;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_tc2_kernel<<<2 * clusters, kThreads, kSmemBytes, stream>>>(a, mq, mkn, mkr, mv);
+  kernel<<<2 * clusters, kThreads, kSmemBytes, stream>>>(a, mq, mkn, mkr, mv);
   count_launch();
   return cudaGetLastError();
 }

@@ -337,9 +337,9 @@ def _lse_rows_batched(got_l, d, rows):
 
 
 @pytest.mark.parametrize("name,tc", [("prefill_bf16", None), ("training_bf16", None), ("long_bf16", None),
-                                     ("prefill_bf16", "2"), ("long_bf16", "1")])
+                                     ("prefill_bf16", "2"), ("long_bf16", "2")])
 def test_full_workload_anchored_sampled(dfl, name, tc, monkeypatch):
-    # default dispatch on every workload, then each workload size on the kernel it does not pick by default
+    # default dispatch on every workload, then the CTA-pair kernel on the shortest and the longest
     if tc:
         monkeypatch.setenv("DFLASH_TC_KERNEL", tc)
     d = synth.make(name)
