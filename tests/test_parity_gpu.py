@@ -103,6 +103,32 @@ def test_small_cases_every_row(dfl, case, mode, kernel):
     assert max_abs_err(got_l, want_l) <= TOL[dtype], name
 
 
+@pytest.mark.parametrize("shape", ["zero", "all_context", "no_context", "unsorted"])
+@pytest.mark.parametrize("mode", ["anchored", "dense"])
+def test_degenerate_anchors_every_row(dfl, shape, mode, kernel):
+    """The extreme cases of the anchored rule on the tensor-core shape: every
+    block sees only itself (all anchors 0), every block sees the whole context
+    (all anchors S), there is no context at all (S = 0), and anchors in no
+    order with repeats (the schedule uses per-tile min/max, not order)."""
+    S = 0 if shape == "no_context" else 500
+    d = synth.make("tiny_fp32", seed=321, dtype="bf16", B=2, H=2, S=S, nb=37, block_size=8, d_nope=128, d_rope=64,
+                   d_v=128, anchor_lo=0, anchor_hi=S + 38)
+    rng = np.random.default_rng(9)
+    if shape in ("zero", "no_context"):
+        d["anchors"][:] = 0
+    elif shape == "all_context":
+        d["anchors"][:] = S
+    else:
+        d["anchors"][:] = rng.integers(0, S + 1, size=d["anchors"].shape).astype(np.int32)
+        d["anchors"][:, 5] = d["anchors"][:, 6]
+    want_o, want_l = oracle.anchored(d["q"], d["k_nope"], d["k_rope"], d["v"], d["anchors"], d["block_size"])
+    mask = _mask_for(d, "bf16") if mode == "dense" else None
+    got_o, got_l = _run_batched(dfl, d, mode, "bf16", mask)
+    assert not np.isnan(got_o).any() and not np.isnan(got_l).any()
+    assert max_abs_err(got_o, want_o) <= TOL["bf16"], shape
+    assert max_abs_err(got_l, want_l) <= TOL["bf16"], shape
+
+
 def test_tiny_fp32_workload_all_entry_points(dfl):
     d = synth.make("tiny_fp32")
     want_o, want_l = oracle.anchored(d["q"], d["k_nope"], d["k_rope"], d["v"], d["anchors"], d["block_size"])
