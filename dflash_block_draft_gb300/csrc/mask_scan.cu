@@ -8,6 +8,7 @@
 // loads when rows are 16-byte aligned.
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dflash {
 namespace {
@@ -24,7 +25,8 @@ __device__ __forceinline__ void classify_bits(uint32_t bits, bool is_bf16, bool&
   }
 }
 
-template <bool kBf16>
+// kVB: bytes per vector load (32 or 16; rows and base aligned to it).
+template <bool kBf16, int kVB>
 __global__ void __launch_bounds__(kScanThreads) mask_scan_kernel(const void* __restrict__ mask, int S, int Q,
                                                                  int nqt, int nkt, bool vec_ok,
                                                                  uint8_t* __restrict__ classes) {
@@ -34,22 +36,29 @@ __global__ void __launch_bounds__(kScanThreads) mask_scan_kernel(const void* __r
   const int c1 = min(c0 + kTileN, K);
   bool all_zero = true, all_ninf = true;
   if (vec_ok && c1 - c0 == kTileN) {
-    // The tile's rows as 16-byte chunks; consecutive threads take consecutive
+    // The tile's rows as kVB-byte chunks; consecutive threads take consecutive
     // chunks of a row, so a warp reads whole rows (coalesced), and every load
     // of a thread is independent of the others.
-    constexpr int kVec = kBf16 ? kTileN * 2 / 16 : kTileN * 4 / 16;  // chunks per row
+    constexpr int kVec = kBf16 ? kTileN * 2 / kVB : kTileN * 4 / kVB;  // chunks per row
 #pragma unroll
     for (int t = 0; t < kVec; ++t) {
       const int c = t * kScanThreads + (int)threadIdx.x;
       const int row = r0 + c / kVec;
       if (row >= Q) continue;
-      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const char*>(mask) +
-                                                      (((size_t)b * Q + row) * (size_t)K + c0) * (kBf16 ? 2 : 4)) +
-                       (c % kVec);
-      const uint4 w = __ldg(p);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      const char* p = static_cast<const char*>(mask) + (((size_t)b * Q + row) * (size_t)K + c0) * (kBf16 ? 2 : 4) +
+                      kVB * (c % kVec);
+      uint32_t ws[kVB / 4];
+      if (kVB == 32) {
+        ptx::ld_global_nc_v8(p, ws);
+      } else {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
+        ws[0] = w.x;
+        ws[1] = w.y;
+        ws[2] = w.z;
+        ws[3] = w.w;
+      }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kVB / 4; ++u) {
         bool z0, n0;
         if (kBf16) {
           bool z1, n1;
@@ -130,12 +139,17 @@ cudaError_t launch_mask_scan(const void* mask, bool bf16, int B, int S, int Q, u
   const int nqt = (Q + kTileM - 1) / kTileM, nkt = (K + kTileN - 1) / kTileN;
   if (B == 0 || nqt == 0 || nkt == 0) return cudaSuccess;
   const size_t esz = bf16 ? 2 : 4;
+  const bool vec32 = ((uintptr_t)mask % 32 == 0) && ((size_t)K * esz) % 32 == 0;
   const bool vec_ok = ((uintptr_t)mask % 16 == 0) && ((size_t)K * esz) % 16 == 0;
   const dim3 grid(nkt, nqt, B);
-  if (bf16)
-    mask_scan_kernel<true><<<grid, kScanThreads, 0, stream>>>(mask, S, Q, nqt, nkt, vec_ok, classes);
+  if (bf16 && vec32)
+    mask_scan_kernel<true, 32><<<grid, kScanThreads, 0, stream>>>(mask, S, Q, nqt, nkt, true, classes);
+  else if (bf16)
+    mask_scan_kernel<true, 16><<<grid, kScanThreads, 0, stream>>>(mask, S, Q, nqt, nkt, vec_ok, classes);
+  else if (vec32)
+    mask_scan_kernel<false, 32><<<grid, kScanThreads, 0, stream>>>(mask, S, Q, nqt, nkt, true, classes);
   else
-    mask_scan_kernel<false><<<grid, kScanThreads, 0, stream>>>(mask, S, Q, nqt, nkt, vec_ok, classes);
+    mask_scan_kernel<false, 16><<<grid, kScanThreads, 0, stream>>>(mask, S, Q, nqt, nkt, vec_ok, classes);
   count_launch();
   return cudaGetLastError();
 }
