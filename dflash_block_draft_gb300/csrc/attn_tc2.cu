@@ -207,7 +207,7 @@ __device__ __forceinline__ int half_class(const Tc2Args& a, const Seg& sg, bool 
   return anchored_tile_class(sg.S, sg.Q, a.p.bs, r0, r1, amin, amax, kt);
 }
 
-// Item index of this cluster's round k (snake order over the longest-first list).
+// Item index of this cluster in its k-th pass over the grid (snake order over the longest-first list).
 __device__ __forceinline__ int item_of_round(int k) {
   const int G = (int)gridDim.x >> 1, c = (int)blockIdx.x >> 1;
   return k * G + ((k & 1) ? (G - 1 - c) : c);
