@@ -6,12 +6,13 @@
  * in one non-causal forward whose keys and values are
  * [projected target-hidden context (S tokens) | noise block (Q tokens)]
  * (nemo_automodel.components.speculative.dflash.draft_kimi_k3 page, module
- * docstring).  Queries are the Q noise (draft) tokens
- * (KimiK3DFlashAttention.forward: "blocks * block_size by sequence +
- * blocks * block_size").  The backbone is Kimi K3 MLA: one K/V per query head
- * with no GQA repeat (KimiK3DFlashAttention), and NoPE: the qk_rope slice of
- * the key is a head-shared extension and no rotary is applied (module
- * docstring).  Per head h, query row i and key k:
+ * docstring).  Queries are the Q noise (draft) tokens: per
+ * KimiK3DFlashAttention.forward the query axis has blocks x block_size rows
+ * and the key axis the sequence plus those rows.  The backbone is Kimi K3
+ * MLA: one K/V per query head with no GQA repeat (KimiK3DFlashAttention), and
+ * NoPE: the rope part of the key is one vector per token, shared by all
+ * heads, with no rotary embedding (module docstring).  Per head h, query row
+ * i and key k:
  *
  *   s(i,k) = ( q_nope(i,h) . k_nope(k,h) + q_rope(i,h) . k_rope(k) ) * scale
  *            [+ mask(i,k) on the dense entry point]

@@ -17,8 +17,8 @@
  *
  * Sources (nemo_automodel.components.speculative.dflash.draft_kimi_k3 page):
  *   - module docstring: keys/values are [target-hidden context | noise block],
- *     one non-causal forward per block; the qk_rope slice of the key is a plain
- *     head-shared extension and no rotary is applied (NoPE);
+ *     one non-causal forward per block; the rope part of the key is one vector
+ *     per token shared by all heads, without rotary embedding (NoPE);
  *   - KimiK3DFlashAttention: one K/V per query head (no GQA repeat);
  *   - KimiK3DFlashAttention.forward: additive mask of shape
  *     [batch, 1, blocks*block_size, sequence + blocks*block_size], passed to
