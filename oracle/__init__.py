@@ -57,9 +57,11 @@ def _load():
             lib.oracle_build_mask.argtypes = [I, I, I, P, I, I, P]
             lib.oracle_tile_classes.argtypes = [I, I, I, I, I, P, I, I, P, I, P]
             lib.oracle_max_threads.argtypes = []
+            lib.oracle_backward.argtypes = [I, I, I, I, I, I, I, D, I, P, P, P, P, P, P, I, I, P, I, P, I64,
+                                            P, P, P, P, I]
             for f in (lib.oracle_dense, lib.oracle_anchored, lib.oracle_ragged,
                       lib.oracle_anchored_split, lib.oracle_build_mask, lib.oracle_tile_classes,
-                      lib.oracle_max_threads):
+                      lib.oracle_max_threads, lib.oracle_backward):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -203,6 +205,46 @@ def anchored_split(q, k_nope, k_rope, v, anchors, block_size, split, scale=None,
     if rc:
         raise ValueError(f"oracle_anchored_split failed ({rc})")
     return out.reshape(B, Q, H, dv), lse.reshape(B, Q, H).transpose(0, 2, 1).copy()
+
+
+def backward(q, k_nope, k_rope, v, dout, anchors=None, block_size=0, mask=None, scale=None, pairs=None,
+             nthreads=0):
+    """Gradients of L = sum(dout * out) for the anchored rule (anchors given) or
+    a dense additive mask (mask given; the mask itself gets no gradient).
+
+    Shapes as for :func:`dense`; dout [B,Q,H,dv].  Returns fp64
+    (dq [B,Q,H,dn+dr], dk_nope [B,S+Q,H,dn], dk_rope [B,S+Q,dr], dv [B,S+Q,H,dv]).
+    pairs: optional flat (b*H + h) subset; other heads' gradients stay 0 and
+    dk_rope sums only the listed heads.
+    """
+    q, k_nope, k_rope, v, dout = (_c(x) for x in (q, k_nope, k_rope, v, dout))
+    B, Q, H, dqk = q.shape
+    S = k_nope.shape[1] - Q
+    dn, dr, dv = k_nope.shape[3], k_rope.shape[2], v.shape[3]
+    assert dn + dr == dqk and dout.shape == (B, Q, H, dv)
+    dt = _same_dtype(q, k_nope, k_rope, v, dout)
+    scale = default_scale(dn, dr) if scale is None else float(scale)
+    an, nb, mdt = None, 0, 0
+    if mask is None:
+        an = _c(anchors, np.int32)
+        nb = an.shape[1]
+        assert nb * block_size == Q
+    else:
+        mask = _c(mask)
+        assert mask.shape == (B, 1, Q, S + Q)
+        mdt = _DT[mask.dtype]
+    p, n = _rows_arg(pairs)
+    K = S + Q
+    dq = np.empty((B, Q, H, dqk), np.float64)
+    dkn = np.empty((B, K, H, dn), np.float64)
+    dkr = np.empty((B, K, dr), np.float64)
+    dvo = np.empty((B, K, H, dv), np.float64)
+    rc = _load().oracle_backward(B, H, S, Q, dn, dr, dv, scale, dt, _ptr(q), _ptr(k_nope), _ptr(k_rope),
+                                 _ptr(v), _ptr(dout), _ptr(an), nb, block_size, _ptr(mask), mdt, _ptr(p), n,
+                                 _ptr(dq), _ptr(dkn), _ptr(dkr), _ptr(dvo), nthreads)
+    if rc:
+        raise ValueError(f"oracle_backward failed ({rc})")
+    return dq, dkn, dkr, dvo
 
 
 def build_mask(anchors, block_size, S):

@@ -357,6 +357,128 @@ int oracle_anchored_split(int B, int H, int S, int Q, int dn, int dr, int dv, do
 }
 
 /* ------------------------------------------------------------------------ */
+/* Backward pass: gradients of the scalar L = sum_{b,i,h} dout(i,h) . out(i,h) */
+/* with respect to q, k_nope, k_rope and v.  Differentiating the forward       */
+/* definition row by row (softmax Jacobian dP/ds = diag(P) - P P^T), for each  */
+/* batch row b, head h and query row i over its visible keys k:               */
+/*   P_k  = softmax_k(s)                                                      */
+/*   dP_k = dout(i,h) . v(k,h)                                                */
+/*   D    = sum_k P_k dP_k                  (equals dout(i,h) . out(i,h))      */
+/*   dS_k = P_k (dP_k - D)                  (dL/ds_k)                          */
+/*   dq(i,h)      = scale * sum_k dS_k [k_nope(k,h) | k_rope(k)]               */
+/*   dk_nope(k,h) += scale * dS_k q_nope(i,h)                                  */
+/*   dk_rope(k)   += scale * dS_k q_rope(i,h)     summed over heads, since one */
+/*                                                k_rope serves every head     */
+/*   dv(k,h)      += P_k dout(i,h)                                             */
+/* Visibility is the anchored rule (anchors != NULL) or the dense mask's       */
+/* non--inf entries (mask != NULL); the mask is a constant input and gets no   */
+/* gradient.  A row that sees no key contributes nothing.                     */
+/* pairs: optional subset of (b*H + h) to evaluate (NULL: all); outputs of     */
+/* other pairs stay 0 and dk_rope sums only the listed heads.                  */
+/* Outputs (fp64, zeroed here): dq [B,Q,H,dn+dr], dkn [B,S+Q,H,dn],            */
+/* dkr [B,S+Q,dr], dvo [B,S+Q,H,dv].                                           */
+/* ------------------------------------------------------------------------ */
+int oracle_backward(int B, int H, int S, int Q, int dn, int dr, int dv, double scale, int dt,
+                    const void* q, const void* kn, const void* kr, const void* v, const void* dout,
+                    const int32_t* anchors, int nb, int bs, const void* mask, int mask_dt,
+                    const int64_t* pairs, int64_t npairs, double* dq, double* dkn, double* dkr,
+                    double* dvo, int nthreads) {
+  if (B < 0 || H <= 0 || S < 0 || Q < 0 || dn < 0 || dr < 0 || dv <= 0) return 1;
+  if (!mask && (!anchors || bs <= 0 || nb * bs != Q)) return 1;
+  const io_t io = {H, dn, dr, dv, dt, scale, q, kn, kr, v};
+  const int K = S + Q, dqk = dn + dr;
+  memset(dq, 0, sizeof(double) * (size_t)B * Q * H * dqk);
+  memset(dkn, 0, sizeof(double) * (size_t)B * K * H * dn);
+  memset(dkr, 0, sizeof(double) * (size_t)B * K * dr);
+  memset(dvo, 0, sizeof(double) * (size_t)B * K * H * dv);
+  const int64_t total = pairs ? npairs : (int64_t)B * H;
+  int bad = 0;
+#pragma omp parallel num_threads(nthreads_or_default(nthreads))
+  {
+    const int Kc = K > 0 ? K : 1;
+    int* rel = (int*)malloc(sizeof(int) * Kc);
+    int* kk = (int*)malloc(sizeof(int) * Kc);
+    double* s = (double*)malloc(sizeof(double) * Kc);
+    double* dS = (double*)malloc(sizeof(double) * Kc);
+    double* dkr_part = (double*)malloc(sizeof(double) * (size_t)Kc * (dr > 0 ? dr : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t w = 0; w < total; ++w) {
+      const int64_t pr = pairs ? pairs[w] : w;
+      if (pr < 0 || pr >= (int64_t)B * H) {
+#pragma omp atomic write
+        bad = 1;
+        continue;
+      }
+      const int b = (int)(pr / H), h = (int)(pr % H);
+      memset(dkr_part, 0, sizeof(double) * (size_t)K * dr);
+      for (int i = 0; i < Q; ++i) {
+        const size_t grow = (size_t)b * Q + i;
+        int n = 0;
+        if (mask) {
+          for (int k = 0; k < K; ++k) {
+            const double mk = ld(mask, mask_dt, grow * (size_t)K + k);
+            if (mk == -INFINITY) continue;
+            kk[n] = k;
+            s[n] = scale * qk_dot(&io, grow, (size_t)b * K + k, h) + mk;
+            ++n;
+          }
+        } else {
+          n = anchored_keys(S, Q, bs, anchors[(size_t)b * nb + i / bs], i, rel);
+          for (int t = 0; t < n; ++t) {
+            kk[t] = rel[t];
+            s[t] = scale * qk_dot(&io, grow, (size_t)b * K + rel[t], h);
+          }
+        }
+        if (n == 0) continue;
+        double m = s[0];
+        for (int t = 1; t < n; ++t)
+          if (s[t] > m) m = s[t];
+        double l = 0.0;
+        for (int t = 0; t < n; ++t) l += exp(s[t] - m);
+        /* P_k (kept in s) and dP_k (kept in dS), then D */
+        const size_t ob = (grow * H + h) * (size_t)dv;
+        double D = 0.0;
+        for (int t = 0; t < n; ++t) {
+          s[t] = exp(s[t] - m) / l;
+          const size_t vb = (((size_t)b * K + kk[t]) * H + h) * (size_t)dv;
+          double dp = 0.0;
+          for (int d = 0; d < dv; ++d) dp += ld(dout, dt, ob + d) * ld(v, dt, vb + d);
+          dS[t] = dp;
+          D += s[t] * dp;
+        }
+        const size_t qb = (grow * H + h) * (size_t)dqk;
+        for (int t = 0; t < n; ++t) {
+          const double g = s[t] * (dS[t] - D);
+          const size_t key = (size_t)b * K + kk[t];
+          const size_t knb = (key * H + h) * (size_t)dn, krb = key * (size_t)dr;
+          for (int d = 0; d < dn; ++d) {
+            dq[qb + d] += scale * g * ld(kn, dt, knb + d);
+            dkn[knb + d] += scale * g * ld(q, dt, qb + d);
+          }
+          for (int d = 0; d < dr; ++d) {
+            dq[qb + dn + d] += scale * g * ld(kr, dt, krb + d);
+            dkr_part[(size_t)kk[t] * dr + d] += scale * g * ld(q, dt, qb + dn + d);
+          }
+          const size_t vb = (key * H + h) * (size_t)dv;
+          for (int d = 0; d < dv; ++d) dvo[vb + d] += s[t] * ld(dout, dt, ob + d);
+        }
+      }
+#pragma omp critical(oracle_dkr)
+      {
+        double* dst = dkr + (size_t)b * K * dr;
+        for (size_t e = 0; e < (size_t)K * dr; ++e) dst[e] += dkr_part[e];
+      }
+    }
+    free(rel);
+    free(kk);
+    free(s);
+    free(dS);
+    free(dkr_part);
+  }
+  return bad ? 2 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* The additive block mask the anchored rule stands for: 0 where visible,      */
 /* -inf elsewhere, laid out [B, 1, Q, S+Q] in fp32.                            */
 /* ------------------------------------------------------------------------ */
