@@ -7,6 +7,7 @@ fallback: if the shared library has not been built, every call raises.
 
 The functions carry the C names:
   dflash_attn_dense, dflash_attn_anchored, dflash_attn_ragged,
+  dflash_attn_dense_backward, dflash_attn_anchored_backward,
   dflash_attn_workspace_size, dflash_build_schedule_host, dflash_scan_mask,
   dflash_last_device_error, dflash_status_string.
 """
@@ -24,6 +25,7 @@ LIB_PATH = _build.LIB_PATH
 
 DFLASH_BF16, DFLASH_FP32 = 0, 1
 MODE_DENSE, MODE_ANCHORED, MODE_RAGGED = 0, 1, 2
+MODE_DENSE_BACKWARD, MODE_ANCHORED_BACKWARD = 3, 4
 TILE_M = TILE_N = 128
 TILE_SKIP, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 
@@ -33,7 +35,8 @@ STATUS = {0: "DFLASH_OK", 1: "DFLASH_ERR_INVALID", 2: "DFLASH_ERR_SHAPE", 3: "DF
 
 EXPORTS = ("dflash_attn_dense", "dflash_attn_anchored", "dflash_attn_ragged", "dflash_attn_workspace_size",
            "dflash_build_schedule_host", "dflash_scan_mask", "dflash_status_string", "dflash_last_device_error",
-           "dflash_kernel_launches", "dflash_attn_dense_noalloc", "dflash_build_mask")
+           "dflash_kernel_launches", "dflash_attn_dense_noalloc", "dflash_build_mask",
+           "dflash_attn_anchored_backward", "dflash_attn_dense_backward")
 
 
 class DFlashError(RuntimeError):
@@ -79,6 +82,10 @@ def load_library(path: str | None = None):
         lib.dflash_build_mask.argtypes = [I, I, I, P, I, I, I, P, P]
         lib.dflash_build_mask.restype = ctypes.c_int
         lib.dflash_attn_dense_noalloc.restype = ctypes.c_int
+        lib.dflash_attn_anchored_backward.argtypes = [DP, I, P, P, P, P, P, I, I, P, P, P, P, P, P, P, P, S, P]
+        lib.dflash_attn_dense_backward.argtypes = [DP, I, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P]
+        lib.dflash_attn_anchored_backward.restype = ctypes.c_int
+        lib.dflash_attn_dense_backward.restype = ctypes.c_int
         lib.dflash_kernel_launches.argtypes = []
         lib.dflash_kernel_launches.restype = ctypes.c_uint64
         for name in ("dflash_attn_dense", "dflash_attn_anchored", "dflash_attn_ragged",
@@ -268,6 +275,65 @@ def dflash_attn_ragged(q, k_nope, k_rope, v, q_offsets, kv_offsets, anchors, blo
                                 _dev_ptr(ws, "workspace"), nbytes, _stream(stream))
     _check("dflash_attn_ragged", st)
     return out
+
+
+def _backward_grads(q, k_nope, k_rope, v, grads):
+    torch = _torch()
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k_nope), torch.empty_like(k_rope), torch.empty_like(v))
+    dq, dkn, dkr, dvv = grads
+    for name, g, ref in (("dq", dq, q), ("dk_nope", dkn, k_nope), ("dk_rope", dkr, k_rope), ("dv", dvv, v)):
+        if g.shape != ref.shape or g.dtype != ref.dtype:
+            raise ValueError(f"{name} must match its input's shape and dtype")
+    return dq, dkn, dkr, dvv
+
+
+def dflash_attn_anchored_backward(q, k_nope, k_rope, v, anchors, block_size, out, lse, dout, grads=None, scale=0.0,
+                                  workspace=None, stream=None):
+    """Gradients (dq, dk_nope, dk_rope, dv) of sum(dout * out) for the anchored
+    forward; out and lse [B,H,Q] fp32 are that forward's outputs.  grads: optional
+    preallocated (dq, dk_nope, dk_rope, dv) shaped like (q, k_nope, k_rope, v)."""
+    torch = _torch()
+    lib = load_library()
+    B, H, S, Q, dn, dr, dv = _batched_shapes(q, k_nope, k_rope, v)
+    dt = _dtype_code(q)
+    nb = anchors.shape[1]
+    dq, dkn, dkr, dvv = _backward_grads(q, k_nope, k_rope, v, grads)
+    nbytes = dflash_attn_workspace_size(MODE_ANCHORED_BACKWARD, B, H, S, Q, dn, dr, dv, dt)
+    ws = _workspace(nbytes, workspace, q.device)
+    d = _dims(B, H, S, Q, dn, dr, dv, scale)
+    st = lib.dflash_attn_anchored_backward(
+        ctypes.byref(d), dt, _dev_ptr(q, "q"), _dev_ptr(k_nope, "k_nope", q.dtype), _dev_ptr(k_rope, "k_rope", q.dtype),
+        _dev_ptr(v, "v", q.dtype), _dev_ptr(anchors, "anchors", torch.int32), nb, int(block_size),
+        _dev_ptr(out, "out", q.dtype), _dev_ptr(lse, "lse", torch.float32), _dev_ptr(dout, "dout", q.dtype),
+        _dev_ptr(dq, "dq"), _dev_ptr(dkn, "dk_nope"), _dev_ptr(dkr, "dk_rope"), _dev_ptr(dvv, "dv"),
+        _dev_ptr(ws, "workspace"), nbytes, _stream(stream))
+    _check("dflash_attn_anchored_backward", st)
+    return dq, dkn, dkr, dvv
+
+
+def dflash_attn_dense_backward(q, k_nope, k_rope, v, mask, out, lse, dout, grads=None, scale=0.0, workspace=None,
+                               stream=None):
+    """Gradients (dq, dk_nope, dk_rope, dv) of sum(dout * out) for the dense
+    forward with additive mask [B,1,Q,S+Q] (the mask gets no gradient)."""
+    torch = _torch()
+    lib = load_library()
+    B, H, S, Q, dn, dr, dv = _batched_shapes(q, k_nope, k_rope, v)
+    dt = _dtype_code(q)
+    if tuple(mask.shape) != (B, 1, Q, S + Q):
+        raise ValueError("mask must be [B,1,Q,S+Q]")
+    dq, dkn, dkr, dvv = _backward_grads(q, k_nope, k_rope, v, grads)
+    nbytes = dflash_attn_workspace_size(MODE_DENSE_BACKWARD, B, H, S, Q, dn, dr, dv, dt)
+    ws = _workspace(nbytes, workspace, q.device)
+    d = _dims(B, H, S, Q, dn, dr, dv, scale)
+    st = lib.dflash_attn_dense_backward(
+        ctypes.byref(d), dt, _dev_ptr(q, "q"), _dev_ptr(k_nope, "k_nope", q.dtype), _dev_ptr(k_rope, "k_rope", q.dtype),
+        _dev_ptr(v, "v", q.dtype), _dev_ptr(mask, "mask", q.dtype), _dev_ptr(out, "out", q.dtype),
+        _dev_ptr(lse, "lse", torch.float32), _dev_ptr(dout, "dout", q.dtype), _dev_ptr(dq, "dq"),
+        _dev_ptr(dkn, "dk_nope"), _dev_ptr(dkr, "dk_rope"), _dev_ptr(dvv, "dv"), _dev_ptr(ws, "workspace"), nbytes,
+        _stream(stream))
+    _check("dflash_attn_dense_backward", st)
+    return dq, dkn, dkr, dvv
 
 
 def dflash_build_schedule_host(B, S, Q, anchors, block_size) -> np.ndarray:

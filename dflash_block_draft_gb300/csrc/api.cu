@@ -67,6 +67,29 @@ Layout layout_batched(int mode, int B, int S, int Q) {
   return L;
 }
 
+// Backward workspace: [ctrl | classes (dense) | D | dk_rope accumulator | tile maxima].
+struct BwdLayout {
+  size_t classes = 0, D = 0, acc = 0, amax = 0, total = 0;
+};
+
+BwdLayout layout_backward(bool dense, int B, int H, int S, int Q, int dr) {
+  BwdLayout L;
+  size_t off = kAlign;
+  if (dense) {
+    const size_t nqt = (size_t)(Q + kTileM - 1) / kTileM, nkt = (size_t)(S + Q + kTileN - 1) / kTileN;
+    L.classes = off;
+    off += round_up((size_t)B * nqt * nkt);
+  }
+  L.D = off;
+  off += round_up(sizeof(float) * (size_t)B * H * Q);
+  L.acc = off;
+  off += round_up(sizeof(float) * (size_t)B * (S + Q) * dr);
+  L.amax = off;
+  off += round_up(sizeof(int) * (size_t)bwd_max_qtiles(B, Q));
+  L.total = off;
+  return L;
+}
+
 Layout layout_ragged(int R, int H, bool decode, int total_kv) {
   Layout L;
   L.total = kAlign + (decode ? round_up(decode_workspace_bytes(R, H, total_kv)) : 0);
@@ -203,6 +226,11 @@ size_t dflash_attn_workspace_size(int mode, const dflash_dims_t* dims, dflash_dt
   if (mode == kDense || mode == kAnchored) {
     if (check_dims(dims) != DFLASH_OK) return 0;
     return layout_batched(mode, dims->B, dims->S, dims->Q).total;
+  }
+  if (mode == DFLASH_MODE_DENSE_BACKWARD || mode == DFLASH_MODE_ANCHORED_BACKWARD) {
+    if (check_dims(dims) != DFLASH_OK) return 0;
+    return layout_backward(mode == DFLASH_MODE_DENSE_BACKWARD, dims->B, dims->H, dims->S, dims->Q, dims->d_rope)
+        .total;
   }
   if (mode == kRagged) {
     if (R <= 0 || check_heads(H, d_nope, d_rope, d_v) != DFLASH_OK || total_q < 0 || total_kv < 0 ||
@@ -355,6 +383,85 @@ dflash_status_t dflash_attn_ragged(int R, int H, int d_nope, int d_rope, int d_v
     return launched(launch_tc(p, R, (max_q_len + kTileM - 1) / kTileM, total_q, total_kv,
                                    (cudaStream_t)stream));
   return launched(launch_attn_simt(p, dtype == DFLASH_BF16, R, max_q_len, (cudaStream_t)stream));
+}
+
+}  // extern "C"
+
+namespace dflash {
+namespace {
+
+// Shared validation and launch of the two backward entry points.
+dflash_status_t backward_common(const dflash_dims_t* dims, dflash_dtype_t dtype, const void* q, const void* kn,
+                                const void* kr, const void* v, const int32_t* anchors, int nb, int bs,
+                                const void* mask, const void* out, const float* lse, const void* dout, void* dq,
+                                void* dkn, void* dkr, void* dv, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  dflash_status_t st;
+  if ((st = check_dtype(dtype)) != DFLASH_OK) return st;
+  if ((st = check_dims(dims)) != DFLASH_OK) return st;
+  const bool dense = mask != nullptr || anchors == nullptr;
+  if (!dense && (bs <= 0 || nb < 0 || (long long)nb * bs != dims->Q)) return DFLASH_ERR_SHAPE;
+  if (dims->d_nope + dims->d_rope > DFLASH_BWD_MAX_DQK || dims->d_v > DFLASH_BWD_MAX_DV)
+    return DFLASH_ERR_UNSUPPORTED;
+  if (dims->B == 0 || (long long)dims->S + dims->Q == 0) return DFLASH_OK;
+  if ((st = check_tensors(q, kn, kr, v, const_cast<void*>(out), lse, dims->d_rope)) != DFLASH_OK) return st;
+  if (!lse || !dout || !dq || !dkn || !dv || (dims->d_rope > 0 && !dkr)) return DFLASH_ERR_INVALID;
+  if (dense && !mask) return DFLASH_ERR_INVALID;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dkn) || !aligned16(dv) ||
+      (dims->d_rope > 0 && !aligned16(dkr)) || (dense && !aligned16(mask)))
+    return DFLASH_ERR_ALIGN;
+  const BwdLayout L = layout_backward(dense, dims->B, dims->H, dims->S, dims->Q, dims->d_rope);
+  if ((st = check_workspace(ws, ws_bytes, L.total)) != DFLASH_OK) return st;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  AttnParams p = base_params(dims->H, dims->d_nope, dims->d_rope, dims->d_v, dims->scale, q, kn, kr, v,
+                             const_cast<void*>(out), nullptr);
+  p.B = dims->B;
+  p.S = dims->S;
+  p.Q = dims->Q;
+  const bool bf16 = dtype == DFLASH_BF16;
+  if (dense) {
+    p.mode = kDense;
+    p.mask = mask;
+    p.classes = w + L.classes;
+    p.nqt = (dims->Q + kTileM - 1) / kTileM;
+    p.nkt = (dims->S + dims->Q + kTileN - 1) / kTileN;
+    if (dims->Q > 0 &&
+        launch_mask_scan(mask, bf16, dims->B, dims->S, dims->Q, w + L.classes, stream) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+  } else {
+    p.mode = kAnchored;
+    p.nb = nb;
+    p.bs = bs;
+    p.anchors = anchors;
+  }
+  return launched(launch_attn_bwd(p, bf16, lse, dout, dq, dkn, dkr, dv, reinterpret_cast<float*>(w + L.D),
+                                  reinterpret_cast<float*>(w + L.acc), reinterpret_cast<int*>(w + L.amax),
+                                  stream));
+}
+
+}  // namespace
+}  // namespace dflash
+
+extern "C" {
+
+dflash_status_t dflash_attn_anchored_backward(const dflash_dims_t* dims, dflash_dtype_t dtype, const void* q,
+                                              const void* k_nope, const void* k_rope, const void* v,
+                                              const int32_t* anchors, int nb, int block_size, const void* out,
+                                              const float* lse, const void* dout, void* dq, void* dk_nope,
+                                              void* dk_rope, void* dv, void* workspace, size_t ws_bytes,
+                                              dflash_stream_t stream) {
+  if (!anchors) return DFLASH_ERR_INVALID;
+  return backward_common(dims, dtype, q, k_nope, k_rope, v, anchors, nb, block_size, nullptr, out, lse, dout, dq,
+                         dk_nope, dk_rope, dv, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+dflash_status_t dflash_attn_dense_backward(const dflash_dims_t* dims, dflash_dtype_t dtype, const void* q,
+                                           const void* k_nope, const void* k_rope, const void* v, const void* mask,
+                                           const void* out, const float* lse, const void* dout, void* dq,
+                                           void* dk_nope, void* dk_rope, void* dv, void* workspace,
+                                           size_t ws_bytes, dflash_stream_t stream) {
+  if (!mask) return DFLASH_ERR_INVALID;
+  return backward_common(dims, dtype, q, k_nope, k_rope, v, nullptr, 0, 0, mask, out, lse, dout, dq, dk_nope,
+                         dk_rope, dv, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
 uint64_t dflash_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -67,6 +67,15 @@ int decode_max_units(int R, int total_kv);
 size_t decode_workspace_bytes(int R, int H, int total_kv);
 cudaError_t launch_attn_decode(const AttnParams& p, void* ws, cudaStream_t stream);
 
+// Backward pass (attn_bwd.cu): prep, dq, dk/dv and rope-finish kernels.
+// Workspace: D [B,H,Q] fp32, dkr_acc [B,S+Q,d_rope] fp32, tile_amax
+// [bwd_max_qtiles(B,Q)] int32; dense calls also need p.classes.
+size_t bwd_smem_bytes(int bt, int dqk, int dv);
+long long bwd_max_qtiles(int B, int Q);
+cudaError_t launch_attn_bwd(const AttnParams& p, bool bf16, const float* lse, const void* dout, void* dq,
+                            void* dkn, void* dkr, void* dv, float* D, float* dkr_acc, int* tile_amax,
+                            cudaStream_t stream);
+
 cudaError_t launch_build_mask(const int32_t* anchors, bool bf16, int B, int S, int Q, int nb, int bs, void* mask,
                               unsigned* err, cudaStream_t stream);
 cudaError_t launch_mask_scan(const void* mask, bool bf16, int B, int S, int Q, uint8_t* classes,

@@ -14,7 +14,8 @@ Recipe (shared by every workload):
   drawn on several threads with a result that does not depend on the thread
   count; bf16 workloads round them to bf16 (nearest, ties to even).
 Anchors are sorted, distinct and uniform without replacement over the stated
-range.  bf16 tensors are carried as uint16 bit patterns.
+range.  bf16 tensors are carried as uint16 bit patterns.  The backward pass
+takes its output gradient dout from the same recipe as tensor id 4.
 """
 from __future__ import annotations
 
@@ -147,7 +148,7 @@ def make(w: Workload | str, seed: int | None = None, **override) -> dict:
     seed = w.seed if seed is None else seed
     rng = np.random.default_rng(seed)
     dqk = w.d_nope + w.d_rope
-    d = dict(workload=w, H=w.H, d_nope=w.d_nope, d_rope=w.d_rope, d_v=w.d_v,
+    d = dict(workload=w, seed=seed, H=w.H, d_nope=w.d_nope, d_rope=w.d_rope, d_v=w.d_v,
              block_size=w.block_size, dtype=w.dtype)
     if w.ragged:
         lo, hi = math.log(w.ctx_lo), math.log(w.ctx_hi)
@@ -173,3 +174,10 @@ def make(w: Workload | str, seed: int | None = None, **override) -> dict:
              k_rope=_normal(seed, 2, (w.B, K, w.d_rope), w.dtype),
              v=_normal(seed, 3, (w.B, K, w.H, w.d_v), w.dtype))
     return d
+
+
+def make_dout(d: dict, seed: int | None = None) -> np.ndarray:
+    """Output gradient dout [B,Q,H,dv] (batched) for the inputs `d` of :func:`make`:
+    standard normals of tensor id 4 under the same seed, in d's dtype."""
+    seed = d["seed"] if seed is None else seed
+    return _normal(seed, 4, (d["B"], d["Q"], d["H"], d["d_v"]), d["dtype"])

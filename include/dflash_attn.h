@@ -187,10 +187,59 @@ DFLASH_API dflash_status_t dflash_attn_dense_noalloc(const dflash_dims_t* dims, 
                                                      const void* v, const void* mask, void* out, float* lse,
                                                      dflash_stream_t stream);
 
-enum { DFLASH_MODE_DENSE = 0, DFLASH_MODE_ANCHORED = 1, DFLASH_MODE_RAGGED = 2 };
+enum {
+  DFLASH_MODE_DENSE = 0,
+  DFLASH_MODE_ANCHORED = 1,
+  DFLASH_MODE_RAGGED = 2,
+  DFLASH_MODE_DENSE_BACKWARD = 3,
+  DFLASH_MODE_ANCHORED_BACKWARD = 4
+};
 
 /*
- * Workspace bytes a call needs.  For DENSE/ANCHORED pass dims (dims->B, S, Q,
+ * Backward pass of the anchored and dense entry points: gradients of the
+ * scalar L = sum over (b, i, h, d) of dout * out.  The DFlash draft is a
+ * trained module (nemo_automodel.components.speculative.dflash.draft_kimi_k3
+ * page, module docstring), so the attention's gradients are needed.  Per head
+ * and query row i over its visible keys k, with P the softmax weights
+ * recomputed from the forward's lse:
+ *   dP(i,k) = dout(i) . v(k),  D(i) = dout(i) . out(i),  dS = P (dP - D)
+ *   dq(i)      = scale * sum_k dS(i,k) [k_nope(k) | k_rope(k)]
+ *   dk_nope(k) = scale * sum_i dS(i,k) q_nope(i)
+ *   dk_rope(k) = scale * sum_h sum_i dS(i,k) q_rope(i)   (one rope key per token
+ *                serves every head, so its gradient is the sum over heads)
+ *   dv(k)      = sum_i P(i,k) dout(i)
+ * The mask (dense) is a constant input and gets no gradient.
+ *   q, k_nope, k_rope, v, anchors/mask: the forward's inputs (same layouts).
+ *   out [B,Q,H,d_v] and lse [B,H,Q] fp32: the forward's outputs for these
+ *     inputs (lse is required here).
+ *   dout [B,Q,H,d_v]: gradient of L with respect to out.
+ *   dq [B,Q,H,d_nope+d_rope], dk_nope [B,S+Q,H,d_nope], dk_rope [B,S+Q,d_rope],
+ *   dv [B,S+Q,H,d_v]: written in dtype; every element is written (keys no row
+ *     sees get 0).
+ *   workspace: >= dflash_attn_workspace_size(DFLASH_MODE_*_BACKWARD, ...)
+ *     bytes, 256-byte aligned, device memory; needs no initialisation.
+ * Limits: d_nope + d_rope <= DFLASH_BWD_MAX_DQK and d_v <= DFLASH_BWD_MAX_DV
+ * (else DFLASH_ERR_UNSUPPORTED).  Device pointers, 16-byte aligned; the call
+ * is asynchronous on `stream` and allocates nothing.  Errors as for the
+ * forward entry points.
+ */
+#define DFLASH_BWD_MAX_DQK 256
+#define DFLASH_BWD_MAX_DV 128
+DFLASH_API dflash_status_t dflash_attn_anchored_backward(
+    const dflash_dims_t* dims, dflash_dtype_t dtype, const void* q, const void* k_nope, const void* k_rope,
+    const void* v, const int32_t* anchors, int nb, int block_size, const void* out, const float* lse,
+    const void* dout, void* dq, void* dk_nope, void* dk_rope, void* dv, void* workspace, size_t ws_bytes,
+    dflash_stream_t stream);
+DFLASH_API dflash_status_t dflash_attn_dense_backward(const dflash_dims_t* dims, dflash_dtype_t dtype,
+                                                      const void* q, const void* k_nope, const void* k_rope,
+                                                      const void* v, const void* mask, const void* out,
+                                                      const float* lse, const void* dout, void* dq,
+                                                      void* dk_nope, void* dk_rope, void* dv, void* workspace,
+                                                      size_t ws_bytes, dflash_stream_t stream);
+
+/*
+ * Workspace bytes a call needs.  For DENSE/ANCHORED (and their _BACKWARD
+ * modes) pass dims (dims->B, S, Q,
  * H, head dims) and ignore the ragged arguments; for RAGGED pass dims = NULL
  * and R, H, head dims via the ragged arguments.  Returns 0 on invalid input.
  */

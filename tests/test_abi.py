@@ -92,6 +92,45 @@ def test_host_validation_rejects_bad_arguments(lib):
                                     1 << 20, None) == 1
 
 
+def test_backward_host_validation_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+    good, ws, big = P(4096), P(1 << 20), 1 << 30
+    bw = lib.dflash_attn_anchored_backward
+    dn = lib.dflash_attn_dense_backward
+    d = _dims(B=1, H=2, S=8, Q=4, dn=16, dr=8, dv=16)
+
+    def anch(dims, dtype=0, q=good, lse=good, dq=good, nb=1, bs=4, ws_bytes=big, anchors=good):
+        return bw(ctypes.byref(dims) if dims is not None else None, dtype, q, good, good, good, anchors, nb, bs,
+                  good, lse, good, dq, good, good, good, ws, ws_bytes, None)
+
+    assert anch(None) == 1                      # null dims
+    assert anch(d, dtype=9) == 3                # unknown dtype
+    assert anch(d, nb=3, bs=2) == 2             # nb * block_size != Q
+    assert anch(d, lse=None) == 1               # lse is required
+    assert anch(d, anchors=None) == 1           # anchors are required
+    assert anch(d, q=P(4100)) == 4              # misaligned input
+    assert anch(d, dq=P(4104)) == 4             # misaligned gradient
+    assert anch(d, ws_bytes=16) == 6            # workspace too small
+    assert anch(_dims(dn=200, dr=64)) == 5      # d_nope + d_rope beyond the backward limit
+    assert anch(_dims(dv=192)) == 5             # d_v beyond the backward limit
+    # dense: the mask is required
+    assert dn(ctypes.byref(d), 0, good, good, good, good, None, good, good, good, good, good, good, good, ws, big,
+              None) == 1
+    # nothing to do: no batch rows
+    d0 = _dims(B=0)
+    assert bw(ctypes.byref(d0), 0, None, None, None, None, good, 1, 4, None, None, None, None, None, None, None,
+              None, 0, None) == 0
+
+
+def test_backward_workspace_size_contract(lib):
+    a = dfl.dflash_attn_workspace_size(dfl.MODE_ANCHORED_BACKWARD, 4, 32, 8192, 8192, 128, 64, 128)
+    dn = dfl.dflash_attn_workspace_size(dfl.MODE_DENSE_BACKWARD, 4, 32, 8192, 8192, 128, 64, 128)
+    # D [B,H,Q] fp32 plus the fp32 dk_rope accumulator [B,S+Q,d_rope]
+    assert a >= 4 * 32 * 8192 * 4 + 4 * 16384 * 64 * 4
+    assert dn >= a + 4 * 64 * 128  # plus one class byte per 128 x 128 mask tile
+    assert dfl.dflash_attn_workspace_size(dfl.MODE_ANCHORED_BACKWARD, -1, 32, 8192, 8192, 128, 64, 128) == 0
+
+
 def test_empty_problems_return_ok_without_launching(lib):
     P = ctypes.c_void_p
     d0 = _dims(B=0)
