@@ -24,6 +24,7 @@
 // 256 threads form a 16 x 16 grid: thread (ty, tx) owns rows ty + 16a and
 // columns tx + 16c of every product it computes.
 #include <math.h>
+#include <stdlib.h>
 
 #include <algorithm>
 
@@ -468,8 +469,17 @@ cudaError_t launch_tiles(const BwdArgs& a, size_t smem, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// bf16 with the Kimi K3 MLA head dims runs on the tensor-core kernels of
+// attn_bwd_tc.cu (DFLASH_FORCE_SIMT=1 keeps it on the CUDA cores, for tests).
+bool use_bwd_tc(const AttnParams& p, bool bf16) {
+  if (!bf16 || !bwd_tc_supported(p.dn, p.dr, p.dv)) return false;
+  if ((long long)p.B * p.Q + 128 >= (1ll << 31) || (long long)p.B * (p.S + p.Q) + 128 >= (1ll << 31)) return false;
+  const char* v = getenv("DFLASH_FORCE_SIMT");
+  return !(v && v[0] && v[0] != '0');
+}
+
 template <typename T>
-cudaError_t launch_bwd_t(const BwdArgs& a0, cudaStream_t stream) {
+cudaError_t launch_bwd_t(const BwdArgs& a0, bool tc, cudaStream_t stream) {
   BwdArgs a = a0;
   const AttnParams& p = a.p;
   const int dqk = p.dn + p.dr;
@@ -477,9 +487,9 @@ cudaError_t launch_bwd_t(const BwdArgs& a0, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
-  const int bt = bwd_smem_bytes(64, dqk, p.dv) <= (size_t)optin ? 64 : 32;
+  const int bt = tc || bwd_smem_bytes(64, dqk, p.dv) <= (size_t)optin ? 64 : 32;
   const size_t smem = bwd_smem_bytes(bt, dqk, p.dv);
-  if (smem > (size_t)optin) return cudaErrorInvalidConfiguration;
+  if (!tc && smem > (size_t)optin) return cudaErrorInvalidConfiguration;
   a.bt = bt;
   a.nqt = (p.Q + bt - 1) / bt;
   a.nkt = (p.S + p.Q + bt - 1) / bt;
@@ -490,7 +500,10 @@ cudaError_t launch_bwd_t(const BwdArgs& a0, cudaStream_t stream) {
   bwd_prep_kernel<T><<<std::max(grid, 1), kBwdThreads, 0, stream>>>(a);
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  e = bt == 64 ? launch_tiles<T, 64>(a, smem, stream) : launch_tiles<T, 32>(a, smem, stream);
+  if (tc)
+    e = launch_attn_bwd_tc(p, a.lse, a.dout, a.dq, a.dkn, a.dvo, a.D, a.dkr_acc, a.tile_amax, stream);
+  else
+    e = bt == 64 ? launch_tiles<T, 64>(a, smem, stream) : launch_tiles<T, 32>(a, smem, stream);
   if (e != cudaSuccess) return e;
   const long long n = (long long)p.B * (p.S + p.Q) * p.dr;
   if (n > 0) {
@@ -520,7 +533,7 @@ cudaError_t launch_attn_bwd(const AttnParams& p, bool bf16, const float* lse, co
   a.tile_amax = tile_amax;
   a.bt = 0;
   a.nqt = a.nkt = 0;
-  return bf16 ? launch_bwd_t<__nv_bfloat16>(a, stream) : launch_bwd_t<float>(a, stream);
+  return bf16 ? launch_bwd_t<__nv_bfloat16>(a, use_bwd_tc(p, true), stream) : launch_bwd_t<float>(a, false, stream);
 }
 
 // Largest query-tile count the backward's tile-maximum array must hold.

@@ -1,0 +1,704 @@
+// attn_bwd_tc.cu -- tensor-core (tcgen05 + TMEM + TMA) backward pass of DFlash
+// block attention for the Kimi K3 MLA head dims (bf16; d_nope = 128, d_rope =
+// 64 head-shared, d_v = 128).
+//
+// Gradients of L = sum dout . out (the forward of KimiK3DFlashAttention on the
+// DFlash Kimi K3 draft page, whose draft is trained), per head, with P the
+// softmax weights recomputed from the forward's lse and D = dout . out:
+//   S = Q K^T,  dP = dO V^T,  dS = P (dP - D)
+//   dQ = scale dS K,   dK = scale dS^T Q,   dV = P^T dO
+// Two kernels, each one CTA per tile, 192 threads: warp 0 issues TMA loads,
+// warp 1 owns TMEM and issues the MMAs, warps 2..5 do the elementwise work
+// (one TMEM lane = one row per thread) and the epilogue.
+//
+// bwd_dq_tc: a 128-row query tile; Q and dO stay in shared memory and 64-key
+// tiles of K and V stream through a three-stage ring.  Per key tile j:
+//   S_j = Q K_j^T, dP_j = dO V_j^T   SS MMAs, M = 128, N = 64   (TMEM, two buffers)
+//   dS_j (bf16) over the head of S_j's buffer                    (elementwise warps)
+//   dQ += dS_j K_j                   TS MMAs, N = 192: K_j read MN-major over its
+//                                    three 64-column panels
+// The MMA warp issues S_{j+1}, dP_{j+1} before dQ_j, so the tensor pipe works on
+// the next tile while the elementwise warps work on this one.
+// TMEM: S buffers [0,64) [64,128), dP buffers [128,192) [192,256), dQ [256,448).
+//
+// bwd_dkdv_tc: a 128-key tile; K and V stay in shared memory and 64-row tiles
+// of Q and dO stream through a three-stage ring.  Per query tile j:
+//   S^T_j = K Q_j^T, dP^T_j = V dO_j^T   SS MMAs, M = 128 keys, N = 64 rows
+//   P^T_j, dS^T_j (bf16) over the head of S^T_j's buffer           (elementwise)
+//   dV += P^T_j dO_j  (N = 128),  dK += dS^T_j Q_j  (N = 192)       TS MMAs
+// S^T has two buffers and dP^T one: dP^T_{j+1} goes out once the elementwise
+// warps have read dP^T_j.  TMEM: S^T [0,64) [64,128), dP^T [128,192),
+// dV [192,320), dK [320,512).  The rope columns of dK are this head's share of
+// the head-shared k_rope gradient and are added into an fp32 accumulator.
+//
+// Key (dq) and query (dkdv) tiles that no row-key pair of the CTA's tile sees
+// are skipped, by the anchored rule or the dense mask's 128 x 128 tile
+// classes.  Every mbarrier wait is bounded; one that runs past its budget
+// records DFLASH_ERR_TIMEOUT and the CTA winds down.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace dflash {
+namespace {
+
+using tc::Ctl;
+using tc::kWaitBudgetNs;
+using tc::range_bits;
+
+constexpr int kDn = 128, kDr = 64, kDqk = 192, kDv = 128;
+constexpr int kThreads = 192;
+constexpr uint32_t kStages = 3;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kP128 = 128 * 128;  // panel: 128 rows x 64 bf16, 128-byte swizzled
+constexpr uint32_t kP64 = 64 * 128;    // panel: 64 rows x 64 bf16
+constexpr uint32_t kStageBytes = 5 * kP64;  // dq: K (3 panels) + V (2); dkdv: Q (3) + dO (2)
+constexpr uint32_t kOffFixed = 0;           // dq: Q (3 x 128 rows) + dO (2); dkdv: K (3) + V (2)
+constexpr uint32_t kOffStage = 5 * kP128;
+constexpr uint32_t kOffCols = kOffStage + kStages * kStageBytes;  // dkdv: per-warp column data
+constexpr uint32_t kColWords = 5 * 64;                             // lse2, D, ctx, nlo, nhi
+constexpr uint32_t kOffBar = kOffCols + 4 * kColWords * 4;
+
+enum {
+  BAR_FIXED = 0,                          // Q+dO (dq) or K+V (dkdv) landed
+  BAR_FULL = 1,                           // kStages: stage landed
+  BAR_EMPTY = BAR_FULL + kStages,         // kStages: stage free
+  BAR_SP = BAR_EMPTY + kStages,           // 2: scores of buffer b computed
+  BAR_DS = BAR_SP + 2,                    // 2: bf16 operands of buffer b written (128 arrivals)
+  BAR_DPFREE = BAR_DS + 2,                // dkdv: dP^T read (128 arrivals)
+  BAR_DONE = BAR_DPFREE + 1,              // all accumulating MMAs completed
+  BAR_DRAIN = BAR_DONE + 1,
+  kNumBars = BAR_DRAIN + 1
+};
+constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;
+constexpr uint32_t kOffAbort = kOffSlot + 4;
+constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr uint32_t kIdScore = ptx::idesc_bf16_f32(128, 64, 0, 0);  // both K-major
+constexpr uint32_t kIdN192 = ptx::idesc_bf16_f32(128, 192, 0, 1);  // B MN-major, three panels
+constexpr uint32_t kIdN128 = ptx::idesc_bf16_f32(128, 128, 0, 1);  // B MN-major, two panels
+
+struct BwdTcArgs {
+  AttnParams p;
+  const float* lse;
+  const float* D;
+  const void* dout;
+  void* dq;
+  void* dkn;
+  void* dvo;
+  float* dkr_acc;
+  const int* tile_amax;  // [B, ceil(Q/64)] largest anchor of each 64-row query tile
+  int nqt64;
+  int mask_vec;  // dense: 16-byte mask loads allowed
+};
+
+__device__ __forceinline__ int clamp_anchor(const AttnParams& p, long long idx) {
+  int a = p.anchors[idx];
+  if (a < 0 || a > p.S) {
+    record_error(p.err, DFLASH_ERR_INVALID);
+    a = a < 0 ? 0 : p.S;
+  }
+  return a;
+}
+
+// Any visible (row, key) pair between query rows [r0, r1) and keys [k0, k1)?
+// amax: the largest anchor of those rows (anchored).
+__device__ __forceinline__ bool pair_needed(const BwdTcArgs& a, int b, int r0, int r1, int k0, int k1, int amax) {
+  const AttnParams& p = a.p;
+  if (p.mode == kDense)
+    return p.classes[((long long)b * p.nqt + r0 / kTileM) * p.nkt + k0 / kTileN] != DFLASH_TILE_SKIP;
+  if (k0 < p.S && k0 < amax) return true;
+  const int u0 = p.S + (r0 / p.bs) * p.bs;
+  const int u1 = p.S + min(((r1 - 1) / p.bs + 1) * p.bs, p.Q);
+  return k0 < u1 && k1 > u0;
+}
+
+struct Smem {
+  uint8_t* base;
+  uint32_t sbase;
+  Ctl ctl;
+  uint32_t* tmem_slot;
+};
+
+__device__ __forceinline__ Smem setup_smem(uint8_t* raw, unsigned* err) {
+  Smem s;
+  s.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  s.sbase = ptx::smem_u32(s.base);
+  s.ctl.bar0 = s.sbase + kOffBar;
+  s.ctl.abort = reinterpret_cast<volatile int*>(s.base + kOffAbort);
+  s.ctl.err = err;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.base + kOffSlot);
+  return s;
+}
+
+__device__ __forceinline__ void init_common(const Smem& s, const CUtensorMap* m0, const CUtensorMap* m1,
+                                            const CUtensorMap* m2, const CUtensorMap* m3, const CUtensorMap* m4) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(s.ctl.bar(BAR_FIXED), 1);
+    for (uint32_t i = 0; i < kStages; ++i) {
+      ptx::mbar_init(s.ctl.bar(BAR_FULL + i), 1);
+      ptx::mbar_init(s.ctl.bar(BAR_EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(s.ctl.bar(BAR_SP + i), 1);
+      ptx::mbar_init(s.ctl.bar(BAR_DS + i), 128);
+    }
+    ptx::mbar_init(s.ctl.bar(BAR_DPFREE), 128);
+    ptx::mbar_init(s.ctl.bar(BAR_DONE), 1);
+    ptx::mbar_init(s.ctl.bar(BAR_DRAIN), 1);
+    *s.ctl.abort = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(m0);
+    ptx::prefetch_tmap(m1);
+    ptx::prefetch_tmap(m2);
+    ptx::prefetch_tmap(m3);
+    ptx::prefetch_tmap(m4);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(s.tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+}
+
+// The MMA thread's last act: wait (bounded) until every MMA it issued has
+// completed, so that TMEM can be released.
+__device__ __forceinline__ void drain(const Smem& s) {
+  ptx::tc_commit(s.ctl.bar(BAR_DRAIN));
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(s.ctl.bar(BAR_DRAIN), 0)) {
+    if (ptx::globaltimer() - t0 > kWaitBudgetNs) {
+      record_error(s.ctl.err, DFLASH_ERR_TIMEOUT);
+      break;
+    }
+  }
+}
+
+__device__ __forceinline__ void teardown(const Smem& s, uint32_t tmem) {
+  ptx::tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Dense mask term in base-2 units (the forward's clamp of huge finite values).
+__device__ __forceinline__ float mask2(float mk) { return mk == -INFINITY ? -INFINITY : fmaxf(mk * kLog2e, -3.0e38f); }
+
+// ============================================================================ dq
+template <bool DENSE>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ BwdTcArgs a, const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmKn,
+                     const __grid_constant__ CUtensorMap tmKr, const __grid_constant__ CUtensorMap tmV) {
+  extern __shared__ uint8_t smem_raw[];
+  const AttnParams& p = a.p;
+  const Smem s = setup_smem(smem_raw, p.err);
+  const Ctl& ctl = s.ctl;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int S = p.S, Q = p.Q, K = S + Q;
+  const int r0 = t * 128, r1 = min(r0 + 128, Q);
+  const int nkt = (K + 63) / 64;
+  int amax = 0;
+  if (!DENSE) {
+    const long long ti = (long long)b * a.nqt64 + 2 * t;
+    amax = a.tile_amax[ti];
+    if (r0 + 64 < Q) amax = max(amax, a.tile_amax[ti + 1]);
+  }
+  auto needed = [&](int kt) { return pair_needed(a, b, r0, r1, kt * 64, min(kt * 64 + 64, K), amax); };
+
+  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV);
+  const uint32_t tmem = *s.tmem_slot;
+  const uint32_t sQ = s.sbase + kOffFixed, sDO = sQ + 3 * kP128, sSt = s.sbase + kOffStage;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA
+      const int qrow = (int)((long long)b * Q + r0);
+      ptx::mbar_arrive_expect_tx(ctl.bar(BAR_FIXED), 5 * kP128);
+      for (int pn = 0; pn < 3; ++pn) ptx::tma_load_3d(sQ + pn * kP128, &tmQ, ctl.bar(BAR_FIXED), 64 * pn, h, qrow);
+      for (int pn = 0; pn < 2; ++pn) ptx::tma_load_3d(sDO + pn * kP128, &tmDO, ctl.bar(BAR_FIXED), 64 * pn, h, qrow);
+      uint32_t j = 0;
+      for (int kt = 0; kt < nkt; ++kt) {
+        if (!needed(kt)) continue;
+        const uint32_t st = j % kStages;
+        if (!ctl.wait(BAR_EMPTY + st, ((j / kStages) & 1u) ^ 1u)) break;
+        const uint32_t fb = ctl.bar(BAR_FULL + st), dst = sSt + st * kStageBytes;
+        const int krow = (int)((long long)b * K + kt * 64);
+        ptx::mbar_arrive_expect_tx(fb, kStageBytes);
+        ptx::tma_load_3d(dst, &tmKn, fb, 0, h, krow);
+        ptx::tma_load_3d(dst + kP64, &tmKn, fb, 64, h, krow);
+        ptx::tma_load_2d(dst + 2 * kP64, &tmKr, fb, 0, krow);
+        ptx::tma_load_3d(dst + 3 * kP64, &tmV, fb, 0, h, krow);
+        ptx::tma_load_3d(dst + 4 * kP64, &tmV, fb, 64, h, krow);
+        ++j;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA
+      const uint64_t dQd = ptx::smem_desc(sQ, 16, 1024), dDOd = ptx::smem_desc(sDO, 16, 1024);
+      const uint64_t dStK = ptx::smem_desc(sSt, 16, 1024);   // stage, K-major (B of S and dP)
+      const uint64_t dStN = ptx::smem_desc(sSt, kP64, 1024);  // stage, MN-major (B of dQ)
+      bool ok = ctl.wait(BAR_FIXED, 0);
+      auto issue_scores = [&](uint32_t jj) -> bool {
+        const uint32_t st = jj % kStages;
+        if (!ctl.wait(BAR_FULL + st, (jj / kStages) & 1u)) return false;
+        ptx::tc_fence_after();
+        const uint32_t dS = tmem + 64u * (jj & 1u), dP = tmem + 128u + 64u * (jj & 1u);
+#pragma unroll
+        for (int ks = 0; ks < kDqk / 16; ++ks) {
+          const uint32_t pn = ks >> 2, sub = (ks & 3) * 32;
+          ptx::mma_ss(dS, dQd + ((pn * kP128 + sub) >> 4), dStK + ((st * kStageBytes + pn * kP64 + sub) >> 4),
+                      kIdScore, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < kDv / 16; ++ks) {
+          const uint32_t pn = ks >> 2, sub = (ks & 3) * 32;
+          ptx::mma_ss(dP, dDOd + ((pn * kP128 + sub) >> 4),
+                      dStK + ((st * kStageBytes + (3 + pn) * kP64 + sub) >> 4), kIdScore, ks > 0);
+        }
+        ptx::tc_commit(ctl.bar(BAR_SP + (jj & 1u)));
+        return true;
+      };
+      auto issue_dq = [&](uint32_t jj) -> bool {
+        const uint32_t st = jj % kStages;
+        if (!ctl.wait(BAR_DS + (jj & 1u), (jj >> 1) & 1u)) return false;
+        ptx::tc_fence_after();
+        const uint32_t aS = tmem + 64u * (jj & 1u);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // 16 keys: 8 packed columns of dS, two 1024-byte row groups of K
+          ptx::mma_ts(tmem + 256u, aS + 8u * ks, dStN + ((st * kStageBytes + ks * 2048u) >> 4), kIdN192,
+                      jj > 0 || ks > 0);
+        ptx::tc_commit(ctl.bar(BAR_EMPTY + st));
+        return true;
+      };
+      uint32_t j = 0;
+      for (int kt = 0; ok && kt < nkt; ++kt) {
+        if (!needed(kt)) continue;
+        ok = issue_scores(j);
+        if (ok && j > 0) ok = issue_dq(j - 1);
+        ++j;
+      }
+      if (ok && j > 0) ok = issue_dq(j - 1);
+      if (ok) ptx::tc_commit(ctl.bar(BAR_DONE));
+      drain(s);
+    }
+  } else {
+    // ------------------------------------------------------------------ elementwise + epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int i = r0 + row;
+    const bool row_ok = i < Q;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const float c2 = p.scale_log2;
+    const long long li = ((long long)b * p.H + h) * Q + i;
+    const float lse2 = row_ok ? a.lse[li] * kLog2e : 0.f;
+    const float Di = row_ok ? a.D[li] : 0.f;
+    int ctx = 0, nlo = 0, nhi = 0;
+    const __nv_bfloat16* mrow = nullptr;
+    if (DENSE) {
+      mrow = static_cast<const __nv_bfloat16*>(p.mask) + ((long long)b * Q + (row_ok ? i : 0)) * (long long)K;
+    } else if (row_ok) {
+      ctx = clamp_anchor(p, (long long)b * p.nb + i / p.bs);
+      const int blk = i / p.bs;
+      nlo = S + blk * p.bs;
+      nhi = S + min(blk * p.bs + p.bs, Q);
+    }
+    uint32_t j = 0;
+    bool ok = true;
+    for (int kt = 0; kt < nkt; ++kt) {
+      if (!needed(kt)) continue;
+      const int k0 = kt * 64;
+      uint64_t vis = 0;
+      if (row_ok) {
+        if (DENSE) vis = range_bits(0, K - k0);
+        else vis = (range_bits(0, ctx - k0) | range_bits(nlo - k0, nhi - k0)) & range_bits(0, K - k0);
+      }
+      // warp-uniform outcome: the warp's lanes leave the loop together
+      if (!__all_sync(0xffffffffu, ctl.wait(BAR_SP + (j & 1u), (j >> 1) & 1u))) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t cS = tmem + lane_off + 64u * (j & 1u), cP = tmem + lane_off + 128u + 64u * (j & 1u);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sx[32], px[32];
+        ptx::tmem_ld32(cS + 32u * hh, sx);
+        ptx::tmem_ld32(cP + 32u * hh, px);
+        ptx::tmem_wait_ld();
+        float mk[32];
+        if (DENSE) {
+          if (a.mask_vec && k0 + 32 * hh + 32 <= K) {
+            const uint4* mp = reinterpret_cast<const uint4*>(mrow + k0 + 32 * hh);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const uint4 w = __ldg(mp + v4);
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                mk[v4 * 8 + 2 * u] = __uint_as_float(ws[u] << 16);
+                mk[v4 * 8 + 2 * u + 1] = __uint_as_float(ws[u] & 0xFFFF0000u);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int k = k0 + 32 * hh + c;
+              mk[c] = (row_ok && k < K) ? __bfloat162float(mrow[k]) : -INFINITY;
+            }
+          }
+        }
+        const uint32_t vw = (uint32_t)(vis >> (32 * hh));
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float g[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float x = __uint_as_float(sx[c + e]);
+            const float m2 = DENSE ? mask2(mk[c + e]) : 0.f;
+            const bool v = ((vw >> (c + e)) & 1u) && m2 != -INFINITY;
+            const float pr = v ? ptx::ex2(fmaf(x, c2, m2) - lse2) : 0.f;
+            g[e] = pr * (__uint_as_float(px[c + e]) - Di);
+          }
+          pk[c / 2] = ptx::pack_bf16x2(g[0], g[1]);
+        }
+        ptx::tmem_st16(cS + 16u * hh, pk);  // dS (bf16 pairs) over S columns already read
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ctl.bar(BAR_DS + (j & 1u)));
+      ++j;
+    }
+    // ---- epilogue: dq = scale * dQ (bf16)
+    if (ok && j > 0 && !__all_sync(0xffffffffu, ctl.wait(BAR_DONE, 0))) ok = false;
+    if (ok) {
+      ptx::tc_fence_after();
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) +
+                                            (((long long)b * Q + (row_ok ? i : 0)) * p.H + h) * (long long)kDqk);
+#pragma unroll 1
+      for (int cc = 0; cc < kDqk; cc += 32) {
+        uint32_t o[32], pk[16];
+        if (j > 0) {
+          ptx::tmem_ld32(tmem + lane_off + 256u + cc, o);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          pk[e / 2] = ptx::pack_bf16x2(__uint_as_float(o[e]) * p.scale, __uint_as_float(o[e + 1]) * p.scale);
+        if (row_ok) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[cc / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+    }
+  }
+  teardown(s, tmem);
+}
+
+// ============================================================================ dk, dv
+template <bool DENSE>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_tc_kernel(const __grid_constant__ BwdTcArgs a, const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmKn,
+                       const __grid_constant__ CUtensorMap tmKr, const __grid_constant__ CUtensorMap tmV) {
+  extern __shared__ uint8_t smem_raw[];
+  const AttnParams& p = a.p;
+  const Smem s = setup_smem(smem_raw, p.err);
+  const Ctl& ctl = s.ctl;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int S = p.S, Q = p.Q, K = S + Q;
+  const int k0 = kt * 128, k1 = min(k0 + 128, K);
+  const int nqt = a.nqt64;
+  auto needed = [&](int t) {
+    const int amax = DENSE ? 0 : a.tile_amax[(long long)b * nqt + t];
+    return pair_needed(a, b, t * 64, min(t * 64 + 64, Q), k0, k1, amax);
+  };
+
+  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV);
+  const uint32_t tmem = *s.tmem_slot;
+  const uint32_t sK = s.sbase + kOffFixed, sV = sK + 3 * kP128, sSt = s.sbase + kOffStage;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA
+      const int krow = (int)((long long)b * K + k0);
+      ptx::mbar_arrive_expect_tx(ctl.bar(BAR_FIXED), 5 * kP128);
+      ptx::tma_load_3d(sK, &tmKn, ctl.bar(BAR_FIXED), 0, h, krow);
+      ptx::tma_load_3d(sK + kP128, &tmKn, ctl.bar(BAR_FIXED), 64, h, krow);
+      ptx::tma_load_2d(sK + 2 * kP128, &tmKr, ctl.bar(BAR_FIXED), 0, krow);
+      ptx::tma_load_3d(sV, &tmV, ctl.bar(BAR_FIXED), 0, h, krow);
+      ptx::tma_load_3d(sV + kP128, &tmV, ctl.bar(BAR_FIXED), 64, h, krow);
+      uint32_t j = 0;
+      for (int t = 0; t < nqt; ++t) {
+        if (!needed(t)) continue;
+        const uint32_t st = j % kStages;
+        if (!ctl.wait(BAR_EMPTY + st, ((j / kStages) & 1u) ^ 1u)) break;
+        const uint32_t fb = ctl.bar(BAR_FULL + st), dst = sSt + st * kStageBytes;
+        const int qrow = (int)((long long)b * Q + t * 64);
+        ptx::mbar_arrive_expect_tx(fb, kStageBytes);
+        for (int pn = 0; pn < 3; ++pn) ptx::tma_load_3d(dst + pn * kP64, &tmQ, fb, 64 * pn, h, qrow);
+        for (int pn = 0; pn < 2; ++pn) ptx::tma_load_3d(dst + (3 + pn) * kP64, &tmDO, fb, 64 * pn, h, qrow);
+        ++j;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA
+      const uint64_t dKd = ptx::smem_desc(sK, 16, 1024), dVd = ptx::smem_desc(sV, 16, 1024);
+      const uint64_t dStK = ptx::smem_desc(sSt, 16, 1024);   // Q/dO stage, K-major (B of S^T, dP^T)
+      const uint64_t dStN = ptx::smem_desc(sSt, kP64, 1024);  // MN-major (B of dK, dV)
+      bool ok = ctl.wait(BAR_FIXED, 0);
+      auto wait_stage = [&](uint32_t jj) -> bool {
+        if (!ctl.wait(BAR_FULL + jj % kStages, (jj / kStages) & 1u)) return false;
+        ptx::tc_fence_after();
+        return true;
+      };
+      auto issue_st = [&](uint32_t jj) {
+        const uint32_t st = jj % kStages;
+#pragma unroll
+        for (int ks = 0; ks < kDqk / 16; ++ks) {
+          const uint32_t pn = ks >> 2, sub = (ks & 3) * 32;
+          ptx::mma_ss(tmem + 64u * (jj & 1u), dKd + ((pn * kP128 + sub) >> 4),
+                      dStK + ((st * kStageBytes + pn * kP64 + sub) >> 4), kIdScore, ks > 0);
+        }
+      };
+      auto issue_dpt = [&](uint32_t jj) {
+        const uint32_t st = jj % kStages;
+#pragma unroll
+        for (int ks = 0; ks < kDv / 16; ++ks) {
+          const uint32_t pn = ks >> 2, sub = (ks & 3) * 32;
+          ptx::mma_ss(tmem + 128u, dVd + ((pn * kP128 + sub) >> 4),
+                      dStK + ((st * kStageBytes + (3 + pn) * kP64 + sub) >> 4), kIdScore, ks > 0);
+        }
+        ptx::tc_commit(ctl.bar(BAR_SP + (jj & 1u)));
+      };
+      auto issue_acc = [&](uint32_t jj) -> bool {
+        const uint32_t st = jj % kStages;
+        if (!ctl.wait(BAR_DS + (jj & 1u), (jj >> 1) & 1u)) return false;
+        ptx::tc_fence_after();
+        const uint32_t aP = tmem + 64u * (jj & 1u), aG = aP + 32u;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {  // 16 query rows per k-step
+          const uint32_t boff = (st * kStageBytes + ks * 2048u) >> 4;
+          ptx::mma_ts(tmem + 192u, aP + 8u * ks, dStN + boff + ((3 * kP64) >> 4), kIdN128, jj > 0 || ks > 0);
+          ptx::mma_ts(tmem + 320u, aG + 8u * ks, dStN + boff, kIdN192, jj > 0 || ks > 0);
+        }
+        ptx::tc_commit(ctl.bar(BAR_EMPTY + st));
+        return true;
+      };
+      uint32_t j = 0;
+      for (int t = 0; ok && t < nqt; ++t) {
+        if (!needed(t)) continue;
+        if (!wait_stage(j)) {
+          ok = false;
+          break;
+        }
+        issue_st(j);
+        if (j > 0) {
+          // dP^T has one buffer: the elementwise warps must have read dP^T(j-1)
+          if (!ctl.wait(BAR_DPFREE, (j - 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+        }
+        issue_dpt(j);
+        if (j > 0 && !issue_acc(j - 1)) {
+          ok = false;
+          break;
+        }
+        ++j;
+      }
+      if (ok && j > 0) ok = issue_acc(j - 1);
+      if (ok) ptx::tc_commit(ctl.bar(BAR_DONE));
+      drain(s);
+    }
+  } else {
+    // ------------------------------------------------------------------ elementwise + epilogue
+    const int quad = warp & 3;
+    const int krow_local = quad * 32 + lane;
+    const int k = k0 + krow_local;
+    const bool key_ok = k < K;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const float c2 = p.scale_log2;
+    // per-warp copy of the query tile's per-row data: lse2, D, ctx, nlo, nhi (64 each)
+    float* cl = reinterpret_cast<float*>(s.base + kOffCols) + quad * kColWords;
+    float* cD = cl + 64;
+    int* cctx = reinterpret_cast<int*>(cl + 128);
+    int* cnlo = cctx + 64;
+    int* cnhi = cnlo + 64;
+    uint32_t j = 0;
+    bool ok = true;
+    for (int t = 0; t < nqt; ++t) {
+      if (!needed(t)) continue;
+      const int r0 = t * 64;
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = lane + 32 * u, i = r0 + c;
+        const bool rok = i < Q;
+        const long long li = ((long long)b * p.H + h) * Q + i;
+        cl[c] = rok ? a.lse[li] * kLog2e : 0.f;
+        cD[c] = rok ? a.D[li] : 0.f;
+        int cx = 0, lo = 0, hi = 0;
+        if (!DENSE && rok) {
+          cx = clamp_anchor(p, (long long)b * p.nb + i / p.bs);
+          const int blk = i / p.bs;
+          lo = S + blk * p.bs;
+          hi = S + min(blk * p.bs + p.bs, Q);
+        }
+        cctx[c] = cx;
+        cnlo[c] = lo;
+        cnhi[c] = hi;
+      }
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, ctl.wait(BAR_SP + (j & 1u), (j >> 1) & 1u))) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t cS = tmem + lane_off + 64u * (j & 1u), cP = tmem + lane_off + 128u;
+      uint32_t pkP[32], pkG[32];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sx[32], px[32];
+        ptx::tmem_ld32(cS + 32u * hh, sx);
+        ptx::tmem_ld32(cP + 32u * hh, px);
+        ptx::tmem_wait_ld();
+        if (hh == 1) {
+          // every column of dP^T(j) is in registers: dP^T(j+1) may overwrite it
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(ctl.bar(BAR_DPFREE));
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float pr[2], g[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = 32 * hh + c + e, i = r0 + col;
+            float m2 = -INFINITY;
+            if (key_ok && i < Q) {
+              if (DENSE) m2 = mask2(__bfloat162float(static_cast<const __nv_bfloat16*>(p.mask)[((long long)b * Q + i) * K + k]));
+              else m2 = (k < cctx[col] || (k >= cnlo[col] && k < cnhi[col])) ? 0.f : -INFINITY;
+            }
+            const float x = __uint_as_float(sx[c + e]);
+            pr[e] = m2 != -INFINITY ? ptx::ex2(fmaf(x, c2, m2) - cl[col]) : 0.f;
+            g[e] = pr[e] * (__uint_as_float(px[c + e]) - cD[col]);
+          }
+          pkP[16 * hh + c / 2] = ptx::pack_bf16x2(pr[0], pr[1]);
+          pkG[16 * hh + c / 2] = ptx::pack_bf16x2(g[0], g[1]);
+        }
+      }
+      ptx::tmem_st32(cS, pkP);        // P^T over columns [0, 32) of the S^T buffer
+      ptx::tmem_st32(cS + 32u, pkG);  // dS^T over columns [32, 64)
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ctl.bar(BAR_DS + (j & 1u)));
+      ++j;
+    }
+    // ---- epilogue: dv, dk_nope (bf16), rope share of dk added into the fp32 accumulator
+    if (ok && j > 0 && !__all_sync(0xffffffffu, ctl.wait(BAR_DONE, 0))) ok = false;
+    if (ok) {
+      ptx::tc_fence_after();
+      const long long kk = (long long)b * K + (key_ok ? k : 0);
+      uint4* dvd = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dvo) + (kk * p.H + h) * (long long)kDv);
+      uint4* dkd = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dkn) + (kk * p.H + h) * (long long)kDn);
+      float4* racc = reinterpret_cast<float4*>(a.dkr_acc + kk * (long long)kDr);
+#pragma unroll 1
+      for (int cc = 0; cc < kDv + kDqk; cc += 32) {
+        uint32_t o[32];
+        if (j > 0) {
+          ptx::tmem_ld32(tmem + lane_off + 192u + cc, o);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (!key_ok) continue;
+        if (cc < kDv + kDn) {
+          const float sc = cc < kDv ? 1.f : p.scale;
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            pk[e / 2] = ptx::pack_bf16x2(__uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc);
+          uint4* dst = cc < kDv ? dvd + cc / 8 : dkd + (cc - kDv) / 8;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        } else if (j > 0) {
+          const int d0 = cc - kDv - kDn;
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            atomicAdd(racc + d0 / 4 + v,
+                      make_float4(__uint_as_float(o[4 * v]) * p.scale, __uint_as_float(o[4 * v + 1]) * p.scale,
+                                  __uint_as_float(o[4 * v + 2]) * p.scale, __uint_as_float(o[4 * v + 3]) * p.scale));
+        }
+      }
+    }
+  }
+  teardown(s, tmem);
+}
+
+}  // namespace
+
+bool bwd_tc_supported(int dn, int dr, int dv) { return dn == kDn && dr == kDr && dv == kDv; }
+
+cudaError_t launch_attn_bwd_tc(const AttnParams& p, const float* lse, const void* dout, void* dq, void* dkn,
+                               void* dv, const float* D, float* dkr_acc, const int* tile_amax64, cudaStream_t stream) {
+  BwdTcArgs a;
+  a.p = p;
+  a.lse = lse;
+  a.D = D;
+  a.dout = dout;
+  a.dq = dq;
+  a.dkn = dkn;
+  a.dvo = dv;
+  a.dkr_acc = dkr_acc;
+  a.tile_amax = tile_amax64;
+  a.nqt64 = (p.Q + 63) / 64;
+  a.mask_vec = 0;
+  if (p.mode == kDense) a.mask_vec = (((uintptr_t)p.mask & 15u) == 0) && ((p.S + p.Q) % 8 == 0);
+  const long long q_rows = (long long)p.B * p.Q, kv_rows = (long long)p.B * (p.S + p.Q);
+  CUtensorMap q128, do128, kn64, kr64, v64, q64, do64, kn128, kr128, v128;
+  if (!make_map_3d(&q128, p.q, q_rows, p.H, kDqk, 128) || !make_map_3d(&do128, dout, q_rows, p.H, kDv, 128) ||
+      !make_map_3d(&kn64, p.kn, kv_rows, p.H, kDn, 64) || !make_map_2d(&kr64, p.kr, kv_rows, kDr, 64) ||
+      !make_map_3d(&v64, p.v, kv_rows, p.H, kDv, 64) || !make_map_3d(&q64, p.q, q_rows, p.H, kDqk, 64) ||
+      !make_map_3d(&do64, dout, q_rows, p.H, kDv, 64) || !make_map_3d(&kn128, p.kn, kv_rows, p.H, kDn, 128) ||
+      !make_map_2d(&kr128, p.kr, kv_rows, kDr, 128) || !make_map_3d(&v128, p.v, kv_rows, p.H, kDv, 128))
+    return cudaErrorInvalidValue;
+  const bool dense = p.mode == kDense;
+  auto kdq = dense ? bwd_dq_tc_kernel<true> : bwd_dq_tc_kernel<false>;
+  auto kkv = dense ? bwd_dkdv_tc_kernel<true> : bwd_dkdv_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) != cudaSuccess)
+    return e;
+  if (p.Q > 0) {
+    kdq<<<dim3((p.Q + 127) / 128, p.H, p.B), kThreads, kSmemBytes, stream>>>(a, q128, do128, kn64, kr64, v64);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  kkv<<<dim3((p.S + p.Q + 127) / 128, p.H, p.B), kThreads, kSmemBytes, stream>>>(a, q64, do64, kn128, kr128, v128);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

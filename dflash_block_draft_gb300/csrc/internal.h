@@ -76,6 +76,13 @@ cudaError_t launch_attn_bwd(const AttnParams& p, bool bf16, const float* lse, co
                             void* dkn, void* dkr, void* dv, float* D, float* dkr_acc, int* tile_amax,
                             cudaStream_t stream);
 
+// Tensor-core backward (attn_bwd_tc.cu) for the Kimi K3 MLA head dims (bf16):
+// dq and dk/dv kernels; D, the zeroed dk_rope accumulator and the 64-row tile
+// maxima come from the prep kernel of attn_bwd.cu.
+bool bwd_tc_supported(int dn, int dr, int dv);
+cudaError_t launch_attn_bwd_tc(const AttnParams& p, const float* lse, const void* dout, void* dq, void* dkn,
+                               void* dv, const float* D, float* dkr_acc, const int* tile_amax64, cudaStream_t stream);
+
 cudaError_t launch_build_mask(const int32_t* anchors, bool bf16, int B, int S, int Q, int nb, int bs, void* mask,
                               unsigned* err, cudaStream_t stream);
 cudaError_t launch_mask_scan(const void* mask, bool bf16, int B, int S, int Q, uint8_t* classes,

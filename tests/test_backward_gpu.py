@@ -25,6 +25,17 @@ RTOL = {"fp32": 1e-5, "bf16": 2.0 ** -7}
 ATOL = {"fp32": 1e-5, "bf16": 2e-2}
 
 
+@pytest.fixture(params=["default", "simt"])
+def kernel(request, monkeypatch):
+    """Default dispatch (tensor-core kernels for bf16 with the Kimi K3 MLA head
+    dims) or the CUDA-core kernels forced for every shape."""
+    if request.param == "simt":
+        monkeypatch.setenv("DFLASH_FORCE_SIMT", "1")
+    else:
+        monkeypatch.delenv("DFLASH_FORCE_SIMT", raising=False)
+    return request.param
+
+
 @pytest.fixture(scope="module")
 def dfl():
     if not torch.cuda.is_available():
@@ -100,14 +111,14 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_anchored_backward_every_element(dfl, case):
+def test_anchored_backward_every_element(dfl, case, kernel):
     _, dtype, B, H, S, nb, bs, dn, dr, dv = case
     d = _case(dtype, B, H, S, nb, bs, dn, dr, dv)
     _compare(_gpu(dfl, d, dtype), _oracle(d), dtype)
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-def test_dense_backward_with_finite_mask_values(dfl, dtype):
+def test_dense_backward_with_finite_mask_values(dfl, dtype, kernel):
     dn, dr, dv = (128, 64, 128) if dtype == "bf16" else (16, 8, 16)
     d = _case(dtype, 2, 2, 140, 9, 16, dn, dr, dv, seed=77)
     dev_mask, ora_mask = _mask(d, dtype, finite_noise=True)
@@ -123,7 +134,7 @@ def test_dense_backward_row_with_no_visible_key(dfl):
     assert np.all(got[0][0, 5] == 0.0)
 
 
-def test_dense_from_anchors_equals_anchored_backward(dfl):
+def test_dense_from_anchors_equals_anchored_backward(dfl, kernel):
     d = _case("bf16", 1, 2, 260, 10, 16, 128, 64, 128, seed=17)
     dev_mask, _ = _mask(d, "bf16")
     a = _gpu(dfl, d, "bf16")
@@ -141,10 +152,33 @@ def test_keys_no_row_sees_get_zero_gradients(dfl):
     assert np.all(got[1][0, 20:90] == 0.0) and np.all(got[2][0, 20:90] == 0.0) and np.all(got[3][0, 20:90] == 0.0)
 
 
-def test_backward_prefill_workload_every_element(dfl):
+_PREFILL = {}
+
+
+def _prefill_case():
+    if not _PREFILL:
+        d = synth.make("prefill_bf16")
+        d["dout"] = synth.make_dout(d)
+        _PREFILL["d"] = d
+        _PREFILL["want"] = _oracle(d)
+    return _PREFILL["d"], _PREFILL["want"]
+
+
+def test_backward_prefill_workload_every_element(dfl, kernel):
     # The bf16 prefill workload at full size (B=1 H=16 S=4096 nb=256
     # block_size=16), every gradient element against the oracle (whose (b, h)
     # pairs run on all host cores).
-    d = synth.make("prefill_bf16")
-    d["dout"] = synth.make_dout(d)
+    d, want = _prefill_case()
+    _compare(_gpu(dfl, d, "bf16"), want, "bf16")
+
+
+@pytest.mark.parametrize("shape", [
+    # B, H, S, nb, bs: query and key tails that are not multiples of 64 or 128
+    (2, 2, 77, 9, 7),
+    (1, 3, 0, 1, 16),     # no context: only noise keys
+    (3, 1, 130, 1, 16),   # one block per batch row; the next row's keys share a tile
+])
+def test_tc_backward_tails_every_element(dfl, shape, kernel):
+    B, H, S, nb, bs = shape
+    d = _case("bf16", B, H, S, nb, bs, 128, 64, 128, seed=sum(shape))
     _compare(_gpu(dfl, d, "bf16"), _oracle(d), "bf16")
