@@ -253,6 +253,7 @@ def run_ours(args):
     dfl.load_library()
 
     workload, dense = args.workload, args.mode == "dense"
+    backward = args.pass_ == "backward"
     d = synth.make(workload)
     B, Q, H, S, bs = d["B"], d["Q"], d["H"], d["S"], d["block_size"]
     dn, dr, dv = d["d_nope"], d["d_rope"], d["d_v"]
@@ -281,6 +282,32 @@ def run_ours(args):
         else:
             dfl.dflash_attn_anchored(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], anchors, bs, out=out,
                                      workspace=ws, stream=stream)
+
+    if backward:
+        # The backward step takes the forward's out and lse (computed here, once,
+        # outside the timed region) and the output gradient dout.
+        lse = torch.empty((B, H, Q), dtype=torch.float32, device=device)
+        if dense:
+            dfl.dflash_attn_dense(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], mask, out=out, lse=lse,
+                                  workspace=ws, stream=stream)
+        else:
+            dfl.dflash_attn_anchored(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], anchors, bs, out=out,
+                                     lse=lse, workspace=ws, stream=stream)
+        dout = to_dev(synth.make_dout(d), "bf16", device)
+        grads = tuple(torch.empty_like(dev[k]) for k in ("q", "k_nope", "k_rope", "v"))
+        bmode = dfl.MODE_DENSE_BACKWARD if dense else dfl.MODE_ANCHORED_BACKWARD
+        bws = torch.empty(dfl.dflash_attn_workspace_size(bmode, B, H, S, Q, dn, dr, dv), dtype=torch.uint8,
+                          device=device)
+        work = dict(work, flops=work["flops"] // metrics.flops_per_pair(dn, dr, dv)
+                    * metrics.backward_flops_per_pair(dn, dr, dv))
+
+        def step():  # noqa: F811
+            if dense:
+                dfl.dflash_attn_dense_backward(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], mask, out, lse,
+                                               dout, grads=grads, workspace=bws, stream=stream)
+            else:
+                dfl.dflash_attn_anchored_backward(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], anchors, bs,
+                                                  out, lse, dout, grads=grads, workspace=bws, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -318,7 +345,7 @@ def run_ours(args):
     traffic = load_traffic()
 
     # end to end through the public API from pinned host buffers
-    headline = workload == WORKLOAD and not dense
+    headline = workload == WORKLOAD and not dense and not backward
     e2e = None
     if not args.no_e2e and headline:
         pinned = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -394,17 +421,23 @@ def run_ours(args):
                "sample": f"the whole {WORKLOAD} workload ({rows.size} rows x {H} heads, {fl / 1e9:.1f} GFLOP "
                          f"unmasked) x {reps}, {total_t:.1f} s"}
 
-    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+    metric = METRIC
+    if backward:
+        metric = ("DFlash block-attn backward TFLOP/s (unmasked FLOPs, 2*(3*d_qk+2*d_v) per visible pair) "
+                  "& % of GB300 bf16 roofline")
+    line = {"metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_desc(d) + (" (dense mask entry point)" if dense else ""),
+            "config": {"workload": workload_desc(d) + (" (dense mask entry point)" if dense else "")
+                       + (" backward (dq, dk_nope, dk_rope, dv)" if backward else ""),
                        "l2": "flushed between timed steps (256 MiB write)",
                        "unmasked_flops_per_step": work["flops"], "algorithmic_bytes_per_step": work["bytes"],
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic if headline else None,
                          "peak_source": f"bf16_tflops ({peak_src})",
-                         "kernel": "mask scan + attention" if dense else "attention (one launch per step)"},
+                         "kernel": ("prep + dq + dk/dv + rope finish" + (" (+ mask scan)" if dense else ""))
+                         if backward else ("mask scan + attention" if dense else "attention (one launch per step)")},
             "pct_bf16_roofline": 100.0 * achieved / peak,
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": int(launches), "clocks": clocks.summary()}
     if rank == 0:
@@ -521,6 +554,9 @@ def main(argv=None):
                          "(decode_bf16 is HBM-bound and reported in GB/s)")
     ap.add_argument("--mode", choices=["anchored", "dense"], default="anchored",
                     help="entry point for the batched workloads")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
+                    help="batched workloads: time the forward call, or the backward call (gradients of "
+                         "q, k_nope, k_rope, v) given the forward's out and lse")
     ap.add_argument("--requests", type=int, default=None,
                     help="decode_bf16 only: draw this many requests instead of 64 (same recipe; "
                          "for profiling captures that must stay small)")

@@ -85,7 +85,7 @@ BwdLayout layout_backward(bool dense, int B, int H, int S, int Q, int dr) {
   L.acc = off;
   off += round_up(sizeof(float) * (size_t)B * (S + Q) * dr);
   L.amax = off;
-  off += round_up(sizeof(int) * (size_t)bwd_max_qtiles(B, Q));
+  off += round_up(2 * sizeof(int) * (size_t)bwd_max_qtiles(B, Q));
   L.total = off;
   return L;
 }

@@ -55,7 +55,8 @@ struct BwdArgs {
   void* dvo;         // [B,S+Q,H,dv]
   float* D;          // [B,H,Q]
   float* dkr_acc;    // [B,S+Q,dr]
-  int* tile_amax;    // [B,nqt] (anchored)
+  int* tile_amax;    // [B,nqt] (anchored): largest anchor of each query tile
+  int* tile_amin;    // [B,nqt] (anchored): smallest anchor of each query tile
   int bt;            // tile edge
   int nqt, nkt;      // query / key tiles of bt
 };
@@ -183,12 +184,14 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_prep_kernel(const BwdArgs a) 
     for (long long e = t0; e < (long long)p.B * a.nqt; e += nt) {
       const int b = (int)(e / a.nqt), t = (int)(e - (long long)b * a.nqt);
       const int r0 = t * a.bt, r1 = min(r0 + a.bt, p.Q);
-      int amax = 0;
+      int amax = 0, amin = p.S;
       for (int j = r0 / p.bs; j <= (r1 - 1) / p.bs; ++j) {
-        const int an = p.anchors[(long long)b * p.nb + j];
-        amax = max(amax, min(max(an, 0), p.S));
+        const int an = min(max(p.anchors[(long long)b * p.nb + j], 0), p.S);
+        amax = max(amax, an);
+        amin = min(amin, an);
       }
       a.tile_amax[e] = amax;
+      a.tile_amin[e] = amin;
     }
   }
 }
@@ -501,7 +504,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a0, bool tc, cudaStream_t stream) {
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (tc)
-    e = launch_attn_bwd_tc(p, a.lse, a.dout, a.dq, a.dkn, a.dvo, a.D, a.dkr_acc, a.tile_amax, stream);
+    e = launch_attn_bwd_tc(p, a.lse, a.dout, a.dq, a.dkn, a.dvo, a.D, a.dkr_acc, a.tile_amax, a.tile_amin,
+                           stream);
   else
     e = bt == 64 ? launch_tiles<T, 64>(a, smem, stream) : launch_tiles<T, 32>(a, smem, stream);
   if (e != cudaSuccess) return e;
@@ -531,6 +535,7 @@ cudaError_t launch_attn_bwd(const AttnParams& p, bool bf16, const float* lse, co
   a.D = D;
   a.dkr_acc = dkr_acc;
   a.tile_amax = tile_amax;
+  a.tile_amin = tile_amax + bwd_max_qtiles(p.B, p.Q);
   a.bt = 0;
   a.nqt = a.nkt = 0;
   return bf16 ? launch_bwd_t<__nv_bfloat16>(a, use_bwd_tc(p, true), stream) : launch_bwd_t<float>(a, false, stream);

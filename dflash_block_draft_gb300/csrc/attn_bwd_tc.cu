@@ -7,9 +7,11 @@
 // softmax weights recomputed from the forward's lse and D = dout . out:
 //   S = Q K^T,  dP = dO V^T,  dS = P (dP - D)
 //   dQ = scale dS K,   dK = scale dS^T Q,   dV = P^T dO
-// Two kernels, each one CTA per tile, 192 threads: warp 0 issues TMA loads,
-// warp 1 owns TMEM and issues the MMAs, warps 2..5 do the elementwise work
-// (one TMEM lane = one row per thread) and the epilogue.
+// Two kernels, each one CTA per tile, 320 threads: warp 0 issues TMA loads,
+// warp 1 owns TMEM and issues the MMAs, warps 2..9 do the elementwise work and
+// the epilogue.  Those are two warps per TMEM lane quarter (one TMEM lane = one
+// row per thread); the two split each tile's 64 columns in halves, so that two
+// warps per sub-partition hide each other's latency.
 //
 // bwd_dq_tc: a 128-row query tile; Q and dO stay in shared memory and 64-key
 // tiles of K and V stream through a three-stage ring.  Per key tile j:
@@ -50,7 +52,8 @@ using tc::kWaitBudgetNs;
 using tc::range_bits;
 
 constexpr int kDn = 128, kDr = 64, kDqk = 192, kDv = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr uint32_t kElemThreads = 256;  // warps 2..9
 constexpr uint32_t kStages = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kP128 = 128 * 128;  // panel: 128 rows x 64 bf16, 128-byte swizzled
@@ -59,16 +62,16 @@ constexpr uint32_t kStageBytes = 5 * kP64;  // dq: K (3 panels) + V (2); dkdv: Q
 constexpr uint32_t kOffFixed = 0;           // dq: Q (3 x 128 rows) + dO (2); dkdv: K (3) + V (2)
 constexpr uint32_t kOffStage = 5 * kP128;
 constexpr uint32_t kOffCols = kOffStage + kStages * kStageBytes;  // dkdv: per-warp column data
-constexpr uint32_t kColWords = 5 * 64;                             // lse2, D, ctx, nlo, nhi
-constexpr uint32_t kOffBar = kOffCols + 4 * kColWords * 4;
+constexpr uint32_t kColWords = 5 * 32;                             // per warp: lse2, D, ctx, nlo, nhi
+constexpr uint32_t kOffBar = kOffCols + 8 * kColWords * 4;
 
 enum {
   BAR_FIXED = 0,                          // Q+dO (dq) or K+V (dkdv) landed
   BAR_FULL = 1,                           // kStages: stage landed
   BAR_EMPTY = BAR_FULL + kStages,         // kStages: stage free
   BAR_SP = BAR_EMPTY + kStages,           // 2: scores of buffer b computed
-  BAR_DS = BAR_SP + 2,                    // 2: bf16 operands of buffer b written (128 arrivals)
-  BAR_DPFREE = BAR_DS + 2,                // dkdv: dP^T read (128 arrivals)
+  BAR_DS = BAR_SP + 2,                    // 2: bf16 operands of buffer b written (256 arrivals)
+  BAR_DPFREE = BAR_DS + 2,                // dkdv: dP^T read (256 arrivals)
   BAR_DONE = BAR_DPFREE + 1,              // all accumulating MMAs completed
   BAR_DRAIN = BAR_DONE + 1,
   kNumBars = BAR_DRAIN + 1
@@ -92,6 +95,7 @@ struct BwdTcArgs {
   void* dvo;
   float* dkr_acc;
   const int* tile_amax;  // [B, ceil(Q/64)] largest anchor of each 64-row query tile
+  const int* tile_amin;  // [B, ceil(Q/64)] smallest anchor of each 64-row query tile
   int nqt64;
   int mask_vec;  // dense: 16-byte mask loads allowed
 };
@@ -146,9 +150,9 @@ __device__ __forceinline__ void init_common(const Smem& s, const CUtensorMap* m0
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(s.ctl.bar(BAR_SP + i), 1);
-      ptx::mbar_init(s.ctl.bar(BAR_DS + i), 128);
+      ptx::mbar_init(s.ctl.bar(BAR_DS + i), kElemThreads);
     }
-    ptx::mbar_init(s.ctl.bar(BAR_DPFREE), 128);
+    ptx::mbar_init(s.ctl.bar(BAR_DPFREE), kElemThreads);
     ptx::mbar_init(s.ctl.bar(BAR_DONE), 1);
     ptx::mbar_init(s.ctl.bar(BAR_DRAIN), 1);
     *s.ctl.abort = 0;
@@ -299,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------------ elementwise + epilogue
     const int quad = warp & 3;
+    const uint32_t half = (uint32_t)(warp - 2) >> 2;  // which 32 of the tile's 64 keys
     const int row = quad * 32 + lane;
     const int i = r0 + row;
     const bool row_ok = i < Q;
@@ -321,11 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int kt = 0; kt < nkt; ++kt) {
       if (!needed(kt)) continue;
-      const int k0 = kt * 64;
-      uint64_t vis = 0;
+      const int k0 = kt * 64 + 32 * (int)half;  // this warp's first key
+      uint32_t vis = 0;
+      bool full_tile = false;  // dense: an all-0 mask tile needs no mask reads
       if (row_ok) {
-        if (DENSE) vis = range_bits(0, K - k0);
-        else vis = (range_bits(0, ctx - k0) | range_bits(nlo - k0, nhi - k0)) & range_bits(0, K - k0);
+        if (DENSE) {
+          vis = (uint32_t)range_bits(0, K - k0);
+          full_tile = p.classes[((long long)b * p.nqt + t) * p.nkt + (kt * 64) / kTileN] == DFLASH_TILE_FULL;
+        } else {
+          vis = (uint32_t)((range_bits(0, ctx - k0) | range_bits(nlo - k0, nhi - k0)) & range_bits(0, K - k0));
+        }
       }
       // warp-uniform outcome: the warp's lanes leave the loop together
       if (!__all_sync(0xffffffffu, ctl.wait(BAR_SP + (j & 1u), (j >> 1) & 1u))) {
@@ -334,64 +344,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_after();
       const uint32_t cS = tmem + lane_off + 64u * (j & 1u), cP = tmem + lane_off + 128u + 64u * (j & 1u);
+      uint32_t sx[32], px[32];
+      ptx::tmem_ld32(cS + 32u * half, sx);
+      ptx::tmem_ld32(cP + 32u * half, px);
+      float mk[32];
+      if (DENSE) {
+        if (full_tile) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t sx[32], px[32];
-        ptx::tmem_ld32(cS + 32u * hh, sx);
-        ptx::tmem_ld32(cP + 32u * hh, px);
-        ptx::tmem_wait_ld();
-        float mk[32];
-        if (DENSE) {
-          if (a.mask_vec && k0 + 32 * hh + 32 <= K) {
-            const uint4* mp = reinterpret_cast<const uint4*>(mrow + k0 + 32 * hh);
+          for (int c = 0; c < 32; ++c) mk[c] = 0.f;
+        } else if (a.mask_vec && k0 + 32 <= K) {
+          const uint4* mp = reinterpret_cast<const uint4*>(mrow + k0);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              const uint4 w = __ldg(mp + v4);
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const uint4 w = __ldg(mp + v4);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                mk[v4 * 8 + 2 * u] = __uint_as_float(ws[u] << 16);
-                mk[v4 * 8 + 2 * u + 1] = __uint_as_float(ws[u] & 0xFFFF0000u);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const int k = k0 + 32 * hh + c;
-              mk[c] = (row_ok && k < K) ? __bfloat162float(mrow[k]) : -INFINITY;
+            for (int u = 0; u < 4; ++u) {
+              mk[v4 * 8 + 2 * u] = __uint_as_float(ws[u] << 16);
+              mk[v4 * 8 + 2 * u + 1] = __uint_as_float(ws[u] & 0xFFFF0000u);
             }
           }
-        }
-        const uint32_t vw = (uint32_t)(vis >> (32 * hh));
-        uint32_t pk[16];
+        } else {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float g[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float x = __uint_as_float(sx[c + e]);
-            const float m2 = DENSE ? mask2(mk[c + e]) : 0.f;
-            const bool v = ((vw >> (c + e)) & 1u) && m2 != -INFINITY;
-            const float pr = v ? ptx::ex2(fmaf(x, c2, m2) - lse2) : 0.f;
-            g[e] = pr * (__uint_as_float(px[c + e]) - Di);
+          for (int c = 0; c < 32; ++c) {
+            const int k = k0 + c;
+            mk[c] = (row_ok && k < K) ? __bfloat162float(mrow[k]) : -INFINITY;
           }
-          pk[c / 2] = ptx::pack_bf16x2(g[0], g[1]);
         }
-        ptx::tmem_st16(cS + 16u * hh, pk);  // dS (bf16 pairs) over S columns already read
       }
+      ptx::tmem_wait_ld();
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float g[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float x = __uint_as_float(sx[c + e]);
+          const float m2 = DENSE ? mask2(mk[c + e]) : 0.f;
+          const bool v = ((vis >> (c + e)) & 1u) && m2 != -INFINITY;
+          const float pr = v ? ptx::ex2(fmaf(x, c2, m2) - lse2) : 0.f;
+          g[e] = pr * (__uint_as_float(px[c + e]) - Di);
+        }
+        pk[c / 2] = ptx::pack_bf16x2(g[0], g[1]);
+      }
+      ptx::tmem_st16(cS + 16u * half, pk);  // dS (bf16 pairs) over S columns already read
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(ctl.bar(BAR_DS + (j & 1u)));
       ++j;
     }
-    // ---- epilogue: dq = scale * dQ (bf16)
+    // ---- epilogue: dq = scale * dQ (bf16); each warp of a lane quarter writes 96 of the 192 columns
     if (ok && j > 0 && !__all_sync(0xffffffffu, ctl.wait(BAR_DONE, 0))) ok = false;
     if (ok) {
       ptx::tc_fence_after();
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) +
                                             (((long long)b * Q + (row_ok ? i : 0)) * p.H + h) * (long long)kDqk);
 #pragma unroll 1
-      for (int cc = 0; cc < kDqk; cc += 32) {
+      for (int cc = 96 * (int)half; cc < 96 * (int)half + 96; cc += 32) {
         uint32_t o[32], pk[16];
         if (j > 0) {
           ptx::tmem_ld32(tmem + lane_off + 256u + cc, o);
@@ -535,30 +544,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------------ elementwise + epilogue
     const int quad = warp & 3;
+    const uint32_t half = (uint32_t)(warp - 2) >> 2;  // which 32 of the query tile's 64 rows
     const int krow_local = quad * 32 + lane;
     const int k = k0 + krow_local;
     const bool key_ok = k < K;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float c2 = p.scale_log2;
-    // per-warp copy of the query tile's per-row data: lse2, D, ctx, nlo, nhi (64 each)
-    float* cl = reinterpret_cast<float*>(s.base + kOffCols) + quad * kColWords;
-    float* cD = cl + 64;
-    int* cctx = reinterpret_cast<int*>(cl + 128);
-    int* cnlo = cctx + 64;
-    int* cnhi = cnlo + 64;
+    // this warp's copy of its 32 query rows' data: lse2, D, ctx, nlo, nhi
+    float* cl = reinterpret_cast<float*>(s.base + kOffCols) + (warp - 2) * kColWords;
+    float* cD = cl + 32;
+    int* cctx = reinterpret_cast<int*>(cl + 64);
+    int* cnlo = cctx + 32;
+    int* cnhi = cnlo + 32;
     uint32_t j = 0;
     bool ok = true;
     for (int t = 0; t < nqt; ++t) {
       if (!needed(t)) continue;
-      const int r0 = t * 64;
+      const int r0 = t * 64 + 32 * (int)half;  // this warp's first query row
+      // every (row, key) pair of the 64 x 128 tile visible: no per-pair mask
+      bool full_tile;
+      if (DENSE)
+        full_tile = t * 64 + 64 <= Q && k1 <= K &&
+                    p.classes[((long long)b * p.nqt + (t * 64) / kTileM) * p.nkt + kt] == DFLASH_TILE_FULL;
+      else
+        full_tile = t * 64 + 64 <= Q && k1 <= S && k1 <= a.tile_amin[(long long)b * nqt + t];
       __syncwarp();
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = lane + 32 * u, i = r0 + c;
+      {
+        const int i = r0 + lane;
         const bool rok = i < Q;
         const long long li = ((long long)b * p.H + h) * Q + i;
-        cl[c] = rok ? a.lse[li] * kLog2e : 0.f;
-        cD[c] = rok ? a.D[li] : 0.f;
+        cl[lane] = rok ? a.lse[li] * kLog2e : 0.f;
+        cD[lane] = rok ? a.D[li] : 0.f;
         int cx = 0, lo = 0, hi = 0;
         if (!DENSE && rok) {
           cx = clamp_anchor(p, (long long)b * p.nb + i / p.bs);
@@ -566,9 +582,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           lo = S + blk * p.bs;
           hi = S + min(blk * p.bs + p.bs, Q);
         }
-        cctx[c] = cx;
-        cnlo[c] = lo;
-        cnhi[c] = hi;
+        cctx[lane] = cx;
+        cnlo[lane] = lo;
+        cnhi[lane] = hi;
       }
       __syncwarp();
       if (!__all_sync(0xffffffffu, ctl.wait(BAR_SP + (j & 1u), (j >> 1) & 1u))) {
@@ -576,46 +592,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t cS = tmem + lane_off + 64u * (j & 1u), cP = tmem + lane_off + 128u;
-      uint32_t pkP[32], pkG[32];
+      const uint32_t cS = tmem + lane_off + 64u * (j & 1u);
+      uint32_t sx[32], px[32];
+      ptx::tmem_ld32(cS + 32u * half, sx);
+      ptx::tmem_ld32(tmem + lane_off + 128u + 32u * half, px);
+      ptx::tmem_wait_ld();
+      // this warp's columns of dP^T(j) are in registers: dP^T(j+1) may overwrite them
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ctl.bar(BAR_DPFREE));
+      uint32_t pkP[16], pkG[16];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t sx[32], px[32];
-        ptx::tmem_ld32(cS + 32u * hh, sx);
-        ptx::tmem_ld32(cP + 32u * hh, px);
-        ptx::tmem_wait_ld();
-        if (hh == 1) {
-          // every column of dP^T(j) is in registers: dP^T(j+1) may overwrite it
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(ctl.bar(BAR_DPFREE));
-        }
+      for (int c = 0; c < 32; c += 2) {
+        float pr[2], g[2];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float pr[2], g[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = 32 * hh + c + e, i = r0 + col;
-            float m2 = -INFINITY;
+        for (int e = 0; e < 2; ++e) {
+          const int col = c + e, i = r0 + col;
+          float m2;
+          if (full_tile) {
+            m2 = 0.f;
+          } else {
+            m2 = -INFINITY;
             if (key_ok && i < Q) {
-              if (DENSE) m2 = mask2(__bfloat162float(static_cast<const __nv_bfloat16*>(p.mask)[((long long)b * Q + i) * K + k]));
-              else m2 = (k < cctx[col] || (k >= cnlo[col] && k < cnhi[col])) ? 0.f : -INFINITY;
+              if (DENSE)
+                m2 = mask2(__bfloat162float(
+                    static_cast<const __nv_bfloat16*>(p.mask)[((long long)b * Q + i) * K + k]));
+              else
+                m2 = (k < cctx[col] || (k >= cnlo[col] && k < cnhi[col])) ? 0.f : -INFINITY;
             }
-            const float x = __uint_as_float(sx[c + e]);
-            pr[e] = m2 != -INFINITY ? ptx::ex2(fmaf(x, c2, m2) - cl[col]) : 0.f;
-            g[e] = pr[e] * (__uint_as_float(px[c + e]) - cD[col]);
           }
-          pkP[16 * hh + c / 2] = ptx::pack_bf16x2(pr[0], pr[1]);
-          pkG[16 * hh + c / 2] = ptx::pack_bf16x2(g[0], g[1]);
+          const float x = __uint_as_float(sx[c + e]);
+          pr[e] = m2 != -INFINITY ? ptx::ex2(fmaf(x, c2, m2) - cl[col]) : 0.f;
+          g[e] = pr[e] * (__uint_as_float(px[c + e]) - cD[col]);
         }
+        pkP[c / 2] = ptx::pack_bf16x2(pr[0], pr[1]);
+        pkG[c / 2] = ptx::pack_bf16x2(g[0], g[1]);
       }
-      ptx::tmem_st32(cS, pkP);        // P^T over columns [0, 32) of the S^T buffer
-      ptx::tmem_st32(cS + 32u, pkG);  // dS^T over columns [32, 64)
+      ptx::tmem_st16(cS + 16u * half, pkP);        // P^T over columns [0, 32) of the S^T buffer
+      ptx::tmem_st16(cS + 32u + 16u * half, pkG);  // dS^T over columns [32, 64)
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(ctl.bar(BAR_DS + (j & 1u)));
       ++j;
     }
-    // ---- epilogue: dv, dk_nope (bf16), rope share of dk added into the fp32 accumulator
+    // ---- epilogue: dv, dk_nope (bf16), rope share of dk added into the fp32 accumulator.
+    // TMEM columns 192.. hold dV (128) then dK (192): ten 32-column chunks, five per warp.
     if (ok && j > 0 && !__all_sync(0xffffffffu, ctl.wait(BAR_DONE, 0))) ok = false;
     if (ok) {
       ptx::tc_fence_after();
@@ -624,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4* dkd = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dkn) + (kk * p.H + h) * (long long)kDn);
       float4* racc = reinterpret_cast<float4*>(a.dkr_acc + kk * (long long)kDr);
 #pragma unroll 1
-      for (int cc = 0; cc < kDv + kDqk; cc += 32) {
+      for (int cc = 160 * (int)half; cc < 160 * (int)half + 160; cc += 32) {
         uint32_t o[32];
         if (j > 0) {
           ptx::tmem_ld32(tmem + lane_off + 192u + cc, o);
@@ -662,7 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool bwd_tc_supported(int dn, int dr, int dv) { return dn == kDn && dr == kDr && dv == kDv; }
 
 cudaError_t launch_attn_bwd_tc(const AttnParams& p, const float* lse, const void* dout, void* dq, void* dkn,
-                               void* dv, const float* D, float* dkr_acc, const int* tile_amax64, cudaStream_t stream) {
+                               void* dv, const float* D, float* dkr_acc, const int* tile_amax64,
+                               const int* tile_amin64, cudaStream_t stream) {
   BwdTcArgs a;
   a.p = p;
   a.lse = lse;
@@ -673,6 +694,7 @@ cudaError_t launch_attn_bwd_tc(const AttnParams& p, const float* lse, const void
   a.dvo = dv;
   a.dkr_acc = dkr_acc;
   a.tile_amax = tile_amax64;
+  a.tile_amin = tile_amin64;
   a.nqt64 = (p.Q + 63) / 64;
   a.mask_vec = 0;
   if (p.mode == kDense) a.mask_vec = (((uintptr_t)p.mask & 15u) == 0) && ((p.S + p.Q) % 8 == 0);

@@ -69,7 +69,8 @@ cudaError_t launch_attn_decode(const AttnParams& p, void* ws, cudaStream_t strea
 
 // Backward pass (attn_bwd.cu): prep, dq, dk/dv and rope-finish kernels.
 // Workspace: D [B,H,Q] fp32, dkr_acc [B,S+Q,d_rope] fp32, tile_amax
-// [bwd_max_qtiles(B,Q)] int32; dense calls also need p.classes.
+// [2 * bwd_max_qtiles(B,Q)] int32 (largest, then smallest anchor of each query
+// tile); dense calls also need p.classes.
 size_t bwd_smem_bytes(int bt, int dqk, int dv);
 long long bwd_max_qtiles(int B, int Q);
 cudaError_t launch_attn_bwd(const AttnParams& p, bool bf16, const float* lse, const void* dout, void* dq,
@@ -81,7 +82,8 @@ cudaError_t launch_attn_bwd(const AttnParams& p, bool bf16, const float* lse, co
 // maxima come from the prep kernel of attn_bwd.cu.
 bool bwd_tc_supported(int dn, int dr, int dv);
 cudaError_t launch_attn_bwd_tc(const AttnParams& p, const float* lse, const void* dout, void* dq, void* dkn,
-                               void* dv, const float* D, float* dkr_acc, const int* tile_amax64, cudaStream_t stream);
+                               void* dv, const float* D, float* dkr_acc, const int* tile_amax64,
+                               const int* tile_amin64, cudaStream_t stream);
 
 cudaError_t launch_build_mask(const int32_t* anchors, bool bf16, int B, int S, int Q, int nb, int bs, void* mask,
                               unsigned* err, cudaStream_t stream);

@@ -2,7 +2,8 @@
 
 Unmasked FLOPs count 2*(d_qk + d_v) per visible (query row, key, head)
 triple -- the two matrix products QK^T and PV restricted to the pairs the
-mask lets through; exp, scaling and the softmax sums are not counted.
+mask lets through; exp, scaling and the softmax sums are not counted.  The
+backward pass counts its five products the same way, 2*(3*d_qk + 2*d_v).
 Algorithmic bytes are what the operation must move at minimum: q once, the
 k_nope/v of every key that some row of the batch row sees once, the
 head-shared k_rope of those keys once (not per head), the mask once (dense),
@@ -15,6 +16,12 @@ import numpy as np
 
 def flops_per_pair(d_nope: int, d_rope: int, d_v: int) -> int:
     return 2 * (d_nope + d_rope + d_v)
+
+
+def backward_flops_per_pair(d_nope: int, d_rope: int, d_v: int) -> int:
+    """Backward: the five products S = QK^T (recomputed), dP = dO V^T, dV = P^T dO,
+    dK = dS^T Q and dQ = dS K over the visible pairs, 2*(3*d_qk + 2*d_v) FLOPs."""
+    return 2 * (3 * (d_nope + d_rope) + 2 * d_v)
 
 
 def anchored_visible_counts(anchors: np.ndarray, S: int, Q: int, block_size: int) -> np.ndarray:
