@@ -16,7 +16,7 @@
 // bwd_dq_tc: a 128-row query tile; Q and dO stay in shared memory and 64-key
 // tiles of K and V stream through a three-stage ring.  Per key tile j:
 //   S_j = Q K_j^T, dP_j = dO V_j^T   SS MMAs, M = 128, N = 64   (TMEM, two buffers)
-//   dS_j (bf16) over the head of S_j's buffer                    (elementwise warps)
+//   dS_j (bf16) over S_j's columns once read                    (elementwise warps)
 //   dQ += dS_j K_j                   TS MMAs, N = 192: K_j read MN-major over its
 //                                    three 64-column panels
 // The MMA warp issues S_{j+1}, dP_{j+1} before dQ_j, so the tensor pipe works on
@@ -26,12 +26,18 @@
 // bwd_dkdv_tc: a 128-key tile; K and V stay in shared memory and 64-row tiles
 // of Q and dO stream through a three-stage ring.  Per query tile j:
 //   S^T_j = K Q_j^T, dP^T_j = V dO_j^T   SS MMAs, M = 128 keys, N = 64 rows
-//   P^T_j, dS^T_j (bf16) over the head of S^T_j's buffer           (elementwise)
+//   P^T_j, dS^T_j (bf16) over S^T_j's columns once read            (elementwise)
 //   dV += P^T_j dO_j  (N = 128),  dK += dS^T_j Q_j  (N = 192)       TS MMAs
 // S^T has two buffers and dP^T one: dP^T_{j+1} goes out once the elementwise
 // warps have read dP^T_j.  TMEM: S^T [0,64) [64,128), dP^T [128,192),
 // dV [192,320), dK [320,512).  The rope columns of dK are this head's share of
 // the head-shared k_rope gradient and are added into an fp32 accumulator.
+// Column ownership: the two warps of a lane quarter read 32 columns each of a
+// 64-column score buffer and write their bf16 results only over their own 32
+// columns (a warp's packed results would otherwise land on columns its
+// partner has not read yet).  Packed column of key/row r: 32 (r / 32) +
+// (r % 32) / 2, plus 16 for dS^T; a 16-wide MMA k-step ks starts at packed
+// column 32 (ks / 2) + 8 (ks % 2).
 //
 // Key (dq) and query (dkdv) tiles that no row-key pair of the CTA's tile sees
 // are skipped, by the anchored rule or the dense mask's 128 x 128 tile
@@ -284,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aS = tmem + 64u * (jj & 1u);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // 16 keys: 8 packed columns of dS, two 1024-byte row groups of K
-          ptx::mma_ts(tmem + 256u, aS + 8u * ks, dStN + ((st * kStageBytes + ks * 2048u) >> 4), kIdN192,
-                      jj > 0 || ks > 0);
+          ptx::mma_ts(tmem + 256u, aS + 32u * (ks >> 1) + 8u * (ks & 1), dStN + ((st * kStageBytes + ks * 2048u) >> 4),
+                      kIdN192, jj > 0 || ks > 0);
         ptx::tc_commit(ctl.bar(BAR_EMPTY + st));
         return true;
       };
@@ -342,11 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      ptx::tc_fence_after();
-      const uint32_t cS = tmem + lane_off + 64u * (j & 1u), cP = tmem + lane_off + 128u + 64u * (j & 1u);
-      uint32_t sx[32], px[32];
-      ptx::tmem_ld32(cS + 32u * half, sx);
-      ptx::tmem_ld32(cP + 32u * half, px);
       float mk[32];
       if (DENSE) {
         if (full_tile) {
@@ -372,6 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      ptx::tc_fence_after();
+      const uint32_t cS = tmem + lane_off + 64u * (j & 1u), cP = tmem + lane_off + 128u + 64u * (j & 1u);
+      uint32_t sx[32], px[32];
+      // nothing between the asynchronous TMEM loads and their wait
+      ptx::tmem_ld32(cS + 32u * half, sx);
+      ptx::tmem_ld32(cP + 32u * half, px);
       ptx::tmem_wait_ld();
       uint32_t pk[16];
 #pragma unroll
@@ -387,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         pk[c / 2] = ptx::pack_bf16x2(g[0], g[1]);
       }
-      ptx::tmem_st16(cS + 16u * half, pk);  // dS (bf16 pairs) over S columns already read
+      ptx::tmem_st16(cS + 32u * half, pk);  // dS (bf16 pairs) over this warp's S columns, already read
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(ctl.bar(BAR_DS + (j & 1u)));
@@ -504,12 +511,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = jj % kStages;
         if (!ctl.wait(BAR_DS + (jj & 1u), (jj >> 1) & 1u)) return false;
         ptx::tc_fence_after();
-        const uint32_t aP = tmem + 64u * (jj & 1u), aG = aP + 32u;
+        const uint32_t aP = tmem + 64u * (jj & 1u);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {  // 16 query rows per k-step
           const uint32_t boff = (st * kStageBytes + ks * 2048u) >> 4;
-          ptx::mma_ts(tmem + 192u, aP + 8u * ks, dStN + boff + ((3 * kP64) >> 4), kIdN128, jj > 0 || ks > 0);
-          ptx::mma_ts(tmem + 320u, aG + 8u * ks, dStN + boff, kIdN192, jj > 0 || ks > 0);
+          const uint32_t acol = aP + 32u * (ks >> 1) + 8u * (ks & 1);
+          ptx::mma_ts(tmem + 192u, acol, dStN + boff + ((3 * kP64) >> 4), kIdN128, jj > 0 || ks > 0);
+          ptx::mma_ts(tmem + 320u, acol + 16u, dStN + boff, kIdN192, jj > 0 || ks > 0);
         }
         ptx::tc_commit(ctl.bar(BAR_EMPTY + st));
         return true;
@@ -556,10 +564,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* cctx = reinterpret_cast<int*>(cl + 64);
     int* cnlo = cctx + 32;
     int* cnhi = cnlo + 32;
+    // The per-row data of the next query tile is loaded one tile ahead, so that its
+    // memory latency overlaps this tile's work.
+    struct RowData {
+      float l, d;
+      int ctx, lo, hi;
+    };
+    auto load_row = [&](int t) {
+      RowData r{0.f, 0.f, 0, 0, 0};
+      const int i = t * 64 + 32 * (int)half + lane;
+      if (t < nqt && i < Q) {
+        const long long li = ((long long)b * p.H + h) * Q + i;
+        r.l = a.lse[li] * kLog2e;
+        r.d = a.D[li];
+        if (!DENSE) {
+          r.ctx = clamp_anchor(p, (long long)b * p.nb + i / p.bs);
+          const int blk = i / p.bs;
+          r.lo = S + blk * p.bs;
+          r.hi = S + min(blk * p.bs + p.bs, Q);
+        }
+      }
+      return r;
+    };
+    auto next_needed = [&](int t) {
+      for (++t; t < nqt; ++t)
+        if (needed(t)) break;
+      return t;
+    };
     uint32_t j = 0;
     bool ok = true;
-    for (int t = 0; t < nqt; ++t) {
-      if (!needed(t)) continue;
+    int t = next_needed(-1);
+    RowData nxt = load_row(t);
+    for (; t < nqt;) {
+      const int t_after = next_needed(t);
       const int r0 = t * 64 + 32 * (int)half;  // this warp's first query row
       // every (row, key) pair of the 64 x 128 tile visible: no per-pair mask
       bool full_tile;
@@ -569,24 +606,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         full_tile = t * 64 + 64 <= Q && k1 <= S && k1 <= a.tile_amin[(long long)b * nqt + t];
       __syncwarp();
-      {
-        const int i = r0 + lane;
-        const bool rok = i < Q;
-        const long long li = ((long long)b * p.H + h) * Q + i;
-        cl[lane] = rok ? a.lse[li] * kLog2e : 0.f;
-        cD[lane] = rok ? a.D[li] : 0.f;
-        int cx = 0, lo = 0, hi = 0;
-        if (!DENSE && rok) {
-          cx = clamp_anchor(p, (long long)b * p.nb + i / p.bs);
-          const int blk = i / p.bs;
-          lo = S + blk * p.bs;
-          hi = S + min(blk * p.bs + p.bs, Q);
-        }
-        cctx[lane] = cx;
-        cnlo[lane] = lo;
-        cnhi[lane] = hi;
-      }
+      cl[lane] = nxt.l;
+      cD[lane] = nxt.d;
+      cctx[lane] = nxt.ctx;
+      cnlo[lane] = nxt.lo;
+      cnhi[lane] = nxt.hi;
       __syncwarp();
+      nxt = load_row(t_after);
+      // the warp's 32 rows' lse (base 2) and D, in registers for the element loop
+      float nl[32], dd[32];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 x4 = reinterpret_cast<const float4*>(cl)[v];
+        const float4 d4 = reinterpret_cast<const float4*>(cD)[v];
+        nl[4 * v] = -x4.x;
+        nl[4 * v + 1] = -x4.y;
+        nl[4 * v + 2] = -x4.z;
+        nl[4 * v + 3] = -x4.w;
+        dd[4 * v] = d4.x;
+        dd[4 * v + 1] = d4.y;
+        dd[4 * v + 2] = d4.z;
+        dd[4 * v + 3] = d4.w;
+      }
       if (!__all_sync(0xffffffffu, ctl.wait(BAR_SP + (j & 1u), (j >> 1) & 1u))) {
         ok = false;
         break;
@@ -594,6 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const uint32_t cS = tmem + lane_off + 64u * (j & 1u);
       uint32_t sx[32], px[32];
+      // tcgen05.ld writes its registers asynchronously: nothing may come between
+      // the loads and the wait, or the compiler could copy registers not yet written
       ptx::tmem_ld32(cS + 32u * half, sx);
       ptx::tmem_ld32(tmem + lane_off + 128u + 32u * half, px);
       ptx::tmem_wait_ld();
@@ -606,12 +649,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         float pr[2], g[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int col = c + e, i = r0 + col;
-          float m2;
+          const int col = c + e;
+          const float x = __uint_as_float(sx[col]);
+          float arg;
+          bool vis;
           if (full_tile) {
-            m2 = 0.f;
+            arg = fmaf(x, c2, nl[col]);
+            vis = true;
           } else {
-            m2 = -INFINITY;
+            const int i = r0 + col;
+            float m2 = -INFINITY;
             if (key_ok && i < Q) {
               if (DENSE)
                 m2 = mask2(__bfloat162float(
@@ -619,20 +666,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               else
                 m2 = (k < cctx[col] || (k >= cnlo[col] && k < cnhi[col])) ? 0.f : -INFINITY;
             }
+            vis = m2 != -INFINITY;
+            arg = fmaf(x, c2, m2) + nl[col];
           }
-          const float x = __uint_as_float(sx[c + e]);
-          pr[e] = m2 != -INFINITY ? ptx::ex2(fmaf(x, c2, m2) - cl[col]) : 0.f;
-          g[e] = pr[e] * (__uint_as_float(px[c + e]) - cD[col]);
+          pr[e] = vis ? ptx::ex2(arg) : 0.f;
+          g[e] = pr[e] * (__uint_as_float(px[col]) - dd[col]);
         }
         pkP[c / 2] = ptx::pack_bf16x2(pr[0], pr[1]);
         pkG[c / 2] = ptx::pack_bf16x2(g[0], g[1]);
       }
-      ptx::tmem_st16(cS + 16u * half, pkP);        // P^T over columns [0, 32) of the S^T buffer
-      ptx::tmem_st16(cS + 32u + 16u * half, pkG);  // dS^T over columns [32, 64)
+      ptx::tmem_st16(cS + 32u * half, pkP);        // P^T, then dS^T, over this warp's 32 S^T columns
+      ptx::tmem_st16(cS + 32u * half + 16u, pkG);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(ctl.bar(BAR_DS + (j & 1u)));
       ++j;
+      t = t_after;
     }
     // ---- epilogue: dv, dk_nope (bf16), rope share of dk added into the fp32 accumulator.
     // TMEM columns 192.. hold dV (128) then dK (192): ten 32-column chunks, five per warp.
