@@ -9,8 +9,13 @@ d_v=128, inputs N(0,1).  The metric is TFLOP/s over unmasked FLOPs
 (2*(d_qk+d_v) per visible (query, key, head)).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload W] [--mode anchored|dense] [--pass forward|backward]
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent replicas, weak scaling); timing is the max over ranks.
+
+``--pass backward`` times the backward call instead (gradients of q, k_nope,
+k_rope, v given the forward's out and lse), over 2*(3*d_qk + 2*d_v) FLOPs per
+visible pair.
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload (rank 0 only).
