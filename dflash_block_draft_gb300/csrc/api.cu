@@ -391,21 +391,32 @@ namespace dflash {
 namespace {
 
 // Shared validation and launch of the two backward entry points.
-dflash_status_t backward_common(const dflash_dims_t* dims, dflash_dtype_t dtype, const void* q, const void* kn,
-                                const void* kr, const void* v, const int32_t* anchors, int nb, int bs,
-                                const void* mask, const void* out, const float* lse, const void* dout, void* dq,
-                                void* dkn, void* dkr, void* dv, void* ws, size_t ws_bytes, cudaStream_t stream) {
+dflash_status_t backward_common(bool dense, const dflash_dims_t* dims, dflash_dtype_t dtype, const void* q,
+                                const void* kn, const void* kr, const void* v, const int32_t* anchors, int nb,
+                                int bs, const void* mask, const void* out, const float* lse, const void* dout,
+                                void* dq, void* dkn, void* dkr, void* dv, void* ws, size_t ws_bytes,
+                                cudaStream_t stream) {
   dflash_status_t st;
   if ((st = check_dtype(dtype)) != DFLASH_OK) return st;
   if ((st = check_dims(dims)) != DFLASH_OK) return st;
-  const bool dense = mask != nullptr || anchors == nullptr;
   if (!dense && (bs <= 0 || nb < 0 || (long long)nb * bs != dims->Q)) return DFLASH_ERR_SHAPE;
   if (dims->d_nope + dims->d_rope > DFLASH_BWD_MAX_DQK || dims->d_v > DFLASH_BWD_MAX_DV)
     return DFLASH_ERR_UNSUPPORTED;
   if (dims->B == 0 || (long long)dims->S + dims->Q == 0) return DFLASH_OK;
+  if (dims->Q == 0) {
+    // No query row: every key gradient is 0 (q, out, lse, dout and dq are empty).
+    if (!dkn || !dv || (dims->d_rope > 0 && !dkr)) return DFLASH_ERR_INVALID;
+    if (!aligned16(dkn) || !aligned16(dv) || (dims->d_rope > 0 && !aligned16(dkr))) return DFLASH_ERR_ALIGN;
+    const size_t esz = dtype == DFLASH_BF16 ? 2 : 4;
+    const size_t keys = (size_t)dims->B * dims->S;
+    cudaError_t e = cudaMemsetAsync(dkn, 0, keys * dims->H * dims->d_nope * esz, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, keys * dims->H * dims->d_v * esz, stream);
+    if (e == cudaSuccess && dims->d_rope > 0) e = cudaMemsetAsync(dkr, 0, keys * dims->d_rope * esz, stream);
+    return launched(e);
+  }
   if ((st = check_tensors(q, kn, kr, v, const_cast<void*>(out), lse, dims->d_rope)) != DFLASH_OK) return st;
   if (!lse || !dout || !dq || !dkn || !dv || (dims->d_rope > 0 && !dkr)) return DFLASH_ERR_INVALID;
-  if (dense && !mask) return DFLASH_ERR_INVALID;
+  if ((dense && !mask) || (!dense && !anchors)) return DFLASH_ERR_INVALID;
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dkn) || !aligned16(dv) ||
       (dims->d_rope > 0 && !aligned16(dkr)) || (dense && !aligned16(mask)))
     return DFLASH_ERR_ALIGN;
@@ -449,9 +460,8 @@ dflash_status_t dflash_attn_anchored_backward(const dflash_dims_t* dims, dflash_
                                               const float* lse, const void* dout, void* dq, void* dk_nope,
                                               void* dk_rope, void* dv, void* workspace, size_t ws_bytes,
                                               dflash_stream_t stream) {
-  if (!anchors) return DFLASH_ERR_INVALID;
-  return backward_common(dims, dtype, q, k_nope, k_rope, v, anchors, nb, block_size, nullptr, out, lse, dout, dq,
-                         dk_nope, dk_rope, dv, workspace, ws_bytes, (cudaStream_t)stream);
+  return backward_common(false, dims, dtype, q, k_nope, k_rope, v, anchors, nb, block_size, nullptr, out, lse,
+                         dout, dq, dk_nope, dk_rope, dv, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
 dflash_status_t dflash_attn_dense_backward(const dflash_dims_t* dims, dflash_dtype_t dtype, const void* q,
@@ -459,9 +469,8 @@ dflash_status_t dflash_attn_dense_backward(const dflash_dims_t* dims, dflash_dty
                                            const void* out, const float* lse, const void* dout, void* dq,
                                            void* dk_nope, void* dk_rope, void* dv, void* workspace,
                                            size_t ws_bytes, dflash_stream_t stream) {
-  if (!mask) return DFLASH_ERR_INVALID;
-  return backward_common(dims, dtype, q, k_nope, k_rope, v, nullptr, 0, 0, mask, out, lse, dout, dq, dk_nope,
-                         dk_rope, dv, workspace, ws_bytes, (cudaStream_t)stream);
+  return backward_common(true, dims, dtype, q, k_nope, k_rope, v, nullptr, 0, 0, mask, out, lse, dout, dq,
+                         dk_nope, dk_rope, dv, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
 uint64_t dflash_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -215,7 +215,8 @@ enum {
  *   dout [B,Q,H,d_v]: gradient of L with respect to out.
  *   dq [B,Q,H,d_nope+d_rope], dk_nope [B,S+Q,H,d_nope], dk_rope [B,S+Q,d_rope],
  *   dv [B,S+Q,H,d_v]: written in dtype; every element is written (keys no row
- *     sees get 0).
+ *     sees get 0).  With Q = 0 only the key gradients are written (all 0) and
+ *     the query-side pointers may be null.
  *   workspace: >= dflash_attn_workspace_size(DFLASH_MODE_*_BACKWARD, ...)
  *     bytes, 256-byte aligned, device memory; needs no initialisation.
  * Limits: d_nope + d_rope <= DFLASH_BWD_MAX_DQK and d_v <= DFLASH_BWD_MAX_DV

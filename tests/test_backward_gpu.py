@@ -182,3 +182,48 @@ def test_tc_backward_tails_every_element(dfl, shape, kernel):
     B, H, S, nb, bs = shape
     d = _case("bf16", B, H, S, nb, bs, 128, 64, 128, seed=sum(shape))
     _compare(_gpu(dfl, d, "bf16"), _oracle(d), "bf16")
+
+
+def test_backward_without_query_rows_zeroes_key_gradients(dfl):
+    # nb = 0 blocks: no query row sees anything, so every key gradient is 0
+    B, H, S = 2, 2, 50
+    q = torch.empty((B, 0, H, 192), dtype=torch.bfloat16, device="cuda")
+    kn = torch.randn((B, S, H, 128), device="cuda").to(torch.bfloat16)
+    kr = torch.randn((B, S, 64), device="cuda").to(torch.bfloat16)
+    v = torch.randn((B, S, H, 128), device="cuda").to(torch.bfloat16)
+    an = torch.empty((B, 0), dtype=torch.int32, device="cuda")
+    out = torch.empty((B, 0, H, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H, 0), dtype=torch.float32, device="cuda")
+    grads = (torch.empty_like(q), torch.full_like(kn, float("nan")), torch.full_like(kr, float("nan")),
+             torch.full_like(v, float("nan")))
+    g = dfl.dflash_attn_anchored_backward(q, kn, kr, v, an, 16, out, lse, out, grads=grads)
+    torch.cuda.synchronize()
+    assert dfl.dflash_last_device_error() == 0
+    for x in g[1:]:
+        assert torch.all(x == 0)
+
+
+def test_backward_out_of_range_anchor_is_reported(dfl):
+    d = _case("bf16", 1, 2, 100, 4, 16, 128, 64, 128, seed=8)
+    t = {k: to_torch(d[k], "bf16") for k in ("q", "k_nope", "k_rope", "v", "dout")}
+    out = torch.empty((1, d["Q"], 2, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 2, d["Q"]), dtype=torch.float32, device="cuda")
+    an = torch.from_numpy(d["anchors"]).cuda()
+    dfl.dflash_attn_anchored(t["q"], t["k_nope"], t["k_rope"], t["v"], an, 16, out=out, lse=lse)
+    assert dfl.dflash_last_device_error() == 0
+    an[0, 1] = 10_000  # beyond S
+    dfl.dflash_attn_anchored_backward(t["q"], t["k_nope"], t["k_rope"], t["v"], an, 16, out, lse, t["dout"])
+    assert dfl.dflash_last_device_error() == 1  # DFLASH_ERR_INVALID
+
+
+def test_bf16_dense_backward_row_with_no_visible_key(dfl, kernel):
+    d = _case("bf16", 1, 2, 150, 9, 16, 128, 64, 128, seed=12)
+    bits, widened = _mask(d, "bf16", finite_noise=True)
+    bits = bits.copy()
+    widened = widened.copy()
+    neg = synth.f32_to_bf16_bits(np.array([-np.inf], np.float32))[0]
+    bits[0, 0, 37, :] = neg
+    widened[0, 0, 37, :] = -np.inf
+    got = _gpu(dfl, d, "bf16", mask=bits)
+    _compare(got, _oracle(d, mask=widened), "bf16")
+    assert np.all(got[0][0, 37] == 0.0)
