@@ -5,8 +5,9 @@ through the C ABI, and compares every gradient element with oracle.backward
 on the same seeded inputs.
 
 Tolerances.  fp32: the forward's bar of 1e-5 absolute, plus 1e-5 relative for
-the head-summed dk_rope.  bf16: the gradients are computed in fp32 and rounded
-once to bf16 (half an ulp is 2^-9 relative); D = dout . out uses the forward's
+the head-summed dk_rope.  bf16: the gradients accumulate in fp32 and are
+rounded once to bf16 (half an ulp is 2^-9 relative); on the tensor-core path P
+and dS enter their MMAs as bf16, and D = dout . out uses the forward's
 bf16-rounded out.  The bar is 2e-2 absolute (the forward's bar) plus 2^-7
 relative, which covers the rounding of gradients larger than 1.
 """
