@@ -1,17 +1,28 @@
 #!/usr/bin/env python3
 """Benchmark of the DFlash draft block attention on GB300.
 
-One step = one pass of the hot path over one batch of synthetic input: a
+One step = one pass of the hot path over one batch of synthetic input.  The
+headline is the largest single-GPU workload, bf16 long context: a
 ``dflash_attn_anchored`` call (validation, anchor-derived tile schedule,
-TMA/tcgen05 attention with online softmax, epilogue) on the bf16 prefill
-workload B=1 H=16 S=4096 nb=256 block_size=16 (Q=4096), d_nope=128, d_rope=64,
-d_v=128, inputs N(0,1).  The metric is TFLOP/s over unmasked FLOPs
-(2*(d_qk+d_v) per visible (query, key, head)).
+TMA/tcgen05 attention with online softmax, epilogue) on B=2 H=16 S=32768
+nb=2048 block_size=8 (Q=16384), d_nope=128, d_rope=64, d_v=128, inputs N(0,1),
+the last 5 % of each row's context padding that no anchor reaches.  The metric
+is TFLOP/s over unmasked FLOPs (2*(d_qk+d_v) per visible (query, key, head))
+and its fraction of the measured bf16 dense tensor peak.
+
+The same JSON line carries a ``per_config`` block: every other workload of the
+suite measured the same way on the same GPU -- bf16 prefill and training
+(anchored and dense-mask entry points), long context through the dense mask,
+the ragged serving decode (algorithmic HBM GB/s against the measured HBM
+peak) and the tiny fp32 case (its parity against the fp64 oracle, computed in
+the CPU-baseline leg).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload W] [--mode anchored|dense] [--pass forward|backward]
+                       [--no-per-config] [--no-e2e] [--no-cpu-baseline]
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
-(independent replicas, weak scaling); timing is the max over ranks.
+(independent replicas, weak scaling); timing is the max over ranks, and the
+per-config block is left out.
 
 ``--pass backward`` times the backward call instead (gradients of q, k_nope,
 k_rope, v given the forward's out and lse), over 2*(3*d_qk + 2*d_v) FLOPs per
@@ -39,14 +50,28 @@ sys.path.insert(0, ROOT)
 
 from dflash_block_draft_gb300 import metrics, synth  # noqa: E402
 
-WORKLOAD = "prefill_bf16"
+WORKLOAD = "long_bf16"  # the headline: the largest workload that fits one GPU
 METRIC = "DFlash block-attn TFLOP/s (unmasked FLOPs) & % of GB300 bf16 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# The rest of the suite, reported beside the headline: (workload, entry point).
+PER_CONFIG = (("prefill_bf16", "anchored"), ("prefill_bf16", "dense"), ("training_bf16", "anchored"),
+              ("training_bf16", "dense"), ("long_bf16", "dense"), ("decode_bf16", "ragged"),
+              ("tiny_fp32", "anchored"))
+# Targets: prefill-shaped workloads at >= 50 % of the bf16 tensor peak, the
+# ragged decode at >= 60 % of HBM bandwidth.
+TARGET_FRAC = {"tensor": 0.50, "hbm": 0.60}
 
 
-def workload_desc(d) -> str:
-    return (f"{d['workload'].name}: B={d['B']} H={d['H']} S={d['S']} nb={d['nb']} block_size={d['block_size']} "
-            f"Q={d['Q']} d_nope={d['d_nope']} d_rope={d['d_rope']} d_v={d['d_v']} anchored")
+def workload_desc(d, mode="anchored") -> str:
+    w = d["workload"]
+    if w.ragged:
+        return (f"{w.name}: R={d['R']} requests x {w.nb * w.block_size} rows, "
+                f"H={d['H']}, contexts log-uniform [{w.ctx_lo},{w.ctx_hi}], total_kv={d['total_kv']}")
+    s = (f"{w.name}: B={d['B']} H={d['H']} S={d['S']} nb={d['nb']} block_size={d['block_size']} "
+         f"Q={d['Q']} d_nope={d['d_nope']} d_rope={d['d_rope']} d_v={d['d_v']}")
+    if d.get("pad"):
+        s += f" pad={d['pad']}"
+    return s + (" dense mask" if mode == "dense" else " anchored")
 
 
 def load_peaks():
@@ -184,6 +209,24 @@ def barrier(world: int):
 # ---------------------------------------------------------------------------
 # oracle timing (CPU baseline / reference arm)
 # ---------------------------------------------------------------------------
+def block_stride(d, target_flops: float) -> int:
+    """Stride over blocks so that every stride-th block of each batch row (plus
+    the last) carries about target_flops of unmasked oracle work."""
+    total = metrics.anchored_work(d["anchors"], d["S"], d["Q"], d["H"], d["block_size"], d["d_nope"],
+                                  d["d_rope"], d["d_v"])["flops"]
+    return max(1, int(total // max(target_flops, 1.0)))
+
+
+def stratified_rows(d, stride: int):
+    """Flat query rows (b*Q + i) of every stride-th block of each batch row,
+    the first and the last block included; returns (rows, blocks per row)."""
+    nb, bs, Q, B = d["nb"], d["block_size"], d["Q"], d["B"]
+    blocks = np.unique(np.concatenate([np.arange(0, nb, stride), [nb - 1]]))
+    per_b = (blocks[:, None] * bs + np.arange(bs)[None, :]).reshape(-1)
+    rows = (np.arange(B)[:, None] * Q + per_b[None, :]).reshape(-1)
+    return rows.astype(np.int64), int(blocks.size)
+
+
 def oracle_rows_flops(d, rows):
     counts = metrics.anchored_visible_counts(d["anchors"], d["S"], d["Q"], d["block_size"]).reshape(-1)
     return int(counts[rows].sum()) * d["H"] * metrics.flops_per_pair(d["d_nope"], d["d_rope"], d["d_v"])
@@ -197,6 +240,38 @@ def time_oracle(d, rows):
     return dt, oracle_rows_flops(d, rows), oracle.max_threads()
 
 
+def cpu_baseline_leg(d, tiny_gpu=None, min_seconds=8.0):
+    """The CPU baseline: the fp64 oracle, as it stands, on the host cores, over a
+    deterministic stratified sample of the headline workload (about 8 s of
+    work, repeated until min_seconds have passed).  When tiny_gpu holds the GPU
+    outputs of the tiny fp32 workload, the oracle also evaluates that workload
+    and the leg reports the GPU's max abs error against it."""
+    stride = block_stride(d, 150e9)
+    rows, nblk = stratified_rows(d, stride)
+    total_t, total_f, reps, threads = 0.0, 0, 0, 1
+    while reps == 0 or total_t < min_seconds:
+        dt, fl, threads = time_oracle(d, rows)
+        total_t += dt
+        total_f += fl
+        reps += 1
+    all_flops = metrics.anchored_work(d["anchors"], d["S"], d["Q"], d["H"], d["block_size"], d["d_nope"],
+                                      d["d_rope"], d["d_v"])["flops"]
+    cpu = {"value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "sample": (f"{d['workload'].name}: every {stride}th block of each batch row, first and last included "
+                      f"({nblk} of {d['nb']} blocks per row, {rows.size} query rows x {d['H']} heads, "
+                      f"{fl / 1e9:.1f} GFLOP unmasked = {100.0 * fl / all_flops:.2f} % of the workload) "
+                      f"x {reps}, {total_t:.1f} s")}
+    parity = None
+    if tiny_gpu is not None:
+        import oracle
+        t = tiny_gpu["inputs"]
+        want_o, want_l = oracle.anchored(t["q"], t["k_nope"], t["k_rope"], t["v"], t["anchors"], t["block_size"])
+        eo = float(np.abs(tiny_gpu["out"] - want_o).max())
+        el = float(np.abs(tiny_gpu["lse"] - want_l).max())
+        parity = {"max_abs_err_out": eo, "max_abs_err_lse": el, "tol": 1e-5, "ok": bool(max(eo, el) <= 1e-5)}
+    return cpu, parity
+
+
 def cores_available() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -208,10 +283,12 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    d = synth.make(WORKLOAD)
-    # Each step: every 64th query row of the workload (all heads), ~1.3 GFLOP of oracle work.
-    stride = 64
-    rows = np.arange(0, d["B"] * d["Q"], stride, dtype=np.int64)
+    if args.workload == "decode_bf16":
+        return run_reference_decode(args, world)
+    d = synth.make(args.workload)
+    # Each step: a stratified sample of about 5 GFLOP of oracle work.
+    stride = block_stride(d, 5e9)
+    rows, nblk = stratified_rows(d, stride)
     for _ in range(args.warmup):
         time_oracle(d, rows)
     times, flops, threads = [], 0, 1
@@ -221,15 +298,47 @@ def run_reference(args):
         flops = fl
     ms = 1e3 * sum(times) / len(times)
     value = flops / (ms / 1e3) / 1e12
-    sample = (f"every {stride}th query row of {WORKLOAD} ({rows.size} rows x {d['H']} heads, "
-              f"{flops / 1e9:.2f} GFLOP unmasked per step)")
+    sample = (f"every {stride}th block of each batch row of {args.workload}, first and last included "
+              f"({nblk} blocks per row, {rows.size} query rows x {d['H']} heads, {flops / 1e9:.2f} GFLOP "
+              f"unmasked per step)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(d), "l2": "n/a (host CPU)"},
+            "config": {"workload": workload_desc(d, args.mode), "l2": "n/a (host CPU)"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_decode(args, world):
+    import oracle
+    d = synth.make("decode_bf16")
+    H = d["H"]
+    qo, ko = d["q_offsets"], d["kv_offsets"]
+    reqs = np.arange(0, d["R"], 16)  # every 16th request, all its rows
+    rows = np.concatenate([np.arange(qo[r], qo[r + 1]) for r in reqs]).astype(np.int64)
+    work = metrics.ragged_work(qo, ko, d["anchors"], H, d["block_size"], d["d_nope"], d["d_rope"], d["d_v"])
+    frac = sum(int(ko[r + 1] - ko[r]) for r in reqs) / float(ko[-1])
+    nbytes = work["bytes"] * frac
+
+    def one():
+        t0 = time.perf_counter()
+        oracle.ragged(d["q"], d["k_nope"], d["k_rope"], d["v"], qo, ko, d["anchors"], d["block_size"], rows=rows)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one()
+    ms = 1e3 * sum(one() for _ in range(args.steps)) / args.steps
+    value = nbytes / (ms / 1e3) / 1e9
+    line = {"impl": "reference", "metric": "DFlash block-attn ragged decode: algorithmic HBM GB/s",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(d), "l2": "n/a (host CPU)"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"every 16th request ({reqs.size} of {d['R']}), all rows and heads"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -245,89 +354,24 @@ def to_dev(a, dtype, device):
     return torch.from_numpy(a).to(device)
 
 
-def run_ours(args):
+def timed_loop(step, steps, warmup, device, stream, flush, world, dfl):
+    """W untimed warm-up steps, then K steps each bracketed by CUDA events on the
+    launching stream with an L2 flush (outside the events) before each.  Returns
+    (per-step event times in ms, launches in the timed region, clock summary)."""
     import torch
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    device = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(device)
-    import dflash_block_draft_gb300 as dfl
-    dfl.load_library()
-
-    workload, dense = args.workload, args.mode == "dense"
-    backward = args.pass_ == "backward"
-    d = synth.make(workload)
-    B, Q, H, S, bs = d["B"], d["Q"], d["H"], d["S"], d["block_size"]
-    dn, dr, dv = d["d_nope"], d["d_rope"], d["d_v"]
-    work = metrics.anchored_work(d["anchors"], S, Q, H, bs, dn, dr, dv, esize=2)
-    if dense:  # the mask is read once more; visibility is the same as the anchored rule's
-        work["bytes"] += B * Q * (S + Q) * 2 - d["anchors"].size * 4
-    host = {k: d[k] for k in ("q", "k_nope", "k_rope", "v")}
-    dev = {k: to_dev(v, "bf16", device) for k, v in host.items()}
-    anchors = torch.from_numpy(d["anchors"]).to(device)
-    out = torch.empty((B, Q, H, dv), dtype=torch.bfloat16, device=device)
-    mode_code = dfl.MODE_DENSE if dense else dfl.MODE_ANCHORED
-    ws_bytes = dfl.dflash_attn_workspace_size(mode_code, B, H, S, Q, dn, dr, dv)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream(device)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 256 MiB > 129 MB L2
-    mask = None
-    if dense:  # the additive block mask, built on the device from the anchors (+ padding columns)
-        mask = dfl.dflash_build_mask(anchors, bs, S, dtype=torch.bfloat16)
-        if d.get("pad"):
-            mask[:, :, :, S - d["pad"]:S] = float("-inf")
-
-    def step():
-        if dense:
-            dfl.dflash_attn_dense(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], mask, out=out, workspace=ws,
-                                  stream=stream)
-        else:
-            dfl.dflash_attn_anchored(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], anchors, bs, out=out,
-                                     workspace=ws, stream=stream)
-
-    if backward:
-        # The backward step takes the forward's out and lse (computed here, once,
-        # outside the timed region) and the output gradient dout.
-        lse = torch.empty((B, H, Q), dtype=torch.float32, device=device)
-        if dense:
-            dfl.dflash_attn_dense(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], mask, out=out, lse=lse,
-                                  workspace=ws, stream=stream)
-        else:
-            dfl.dflash_attn_anchored(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], anchors, bs, out=out,
-                                     lse=lse, workspace=ws, stream=stream)
-        dout = to_dev(synth.make_dout(d), "bf16", device)
-        grads = tuple(torch.empty_like(dev[k]) for k in ("q", "k_nope", "k_rope", "v"))
-        bmode = dfl.MODE_DENSE_BACKWARD if dense else dfl.MODE_ANCHORED_BACKWARD
-        bws = torch.empty(dfl.dflash_attn_workspace_size(bmode, B, H, S, Q, dn, dr, dv), dtype=torch.uint8,
-                          device=device)
-        work = dict(work, flops=work["flops"] // metrics.flops_per_pair(dn, dr, dv)
-                    * metrics.backward_flops_per_pair(dn, dr, dv))
-
-        def step():  # noqa: F811
-            if dense:
-                dfl.dflash_attn_dense_backward(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], mask, out, lse,
-                                               dout, grads=grads, workspace=bws, stream=stream)
-            else:
-                dfl.dflash_attn_anchored_backward(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], anchors, bs,
-                                                  out, lse, dout, grads=grads, workspace=bws, stream=stream)
-
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         flush.zero_()
         step()
     torch.cuda.synchronize(device)
     if dfl.dflash_last_device_error() != 0:
         raise RuntimeError("device error during warm-up")
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     clocks = ClockSampler(device.index or 0)
     launches0 = dfl.dflash_kernel_launches()
     barrier(world)
     torch.cuda.synchronize(device)
     clocks.start()
-    for k in range(args.steps):
+    for k in range(steps):
         flush.zero_()  # L2 flushed between timed steps (outside the events)
         ev[k][0].record(stream)
         step()
@@ -336,132 +380,167 @@ def run_ours(args):
     barrier(world)
     clocks.stop()
     launches = dfl.dflash_kernel_launches() - launches0
-    times = [a.elapsed_time(b) for a, b in ev]
-    ms = max_over_ranks(sum(times) / len(times), world, device)
-    value = job_value(work["flops"], world, ms) / 1e12
+    if dfl.dflash_last_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    return [a.elapsed_time(b) for a, b in ev], int(launches), clocks.summary()
 
-    peaks, peak_src = load_peaks()
-    # One kernel per step (anchored): the attention kernel is the whole step, so
-    # its average launch duration is the per-step event time.  The dense entry
-    # point adds the mask scan, whose time is included here.
-    kernel_ms = sum(times) / len(times)
-    achieved = work["flops"] / (kernel_ms / 1e3) / 1e12
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = load_traffic()
 
-    # end to end through the public API from pinned host buffers
-    headline = workload == WORKLOAD and not dense and not backward
-    e2e = None
-    if not args.no_e2e and headline:
-        pinned = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).pin_memory()
-                  for k, v in host.items()}
-        an_h = torch.from_numpy(d["anchors"]).pin_memory()
-        out_h = torch.empty((B, Q, H, dv), dtype=torch.bfloat16).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in pinned.values()) + an_h.numel() * 4
-        d2h = out_h.numel() * out_h.element_size()
+def measure_batched(dfl, d, mode, backward, steps, warmup, device, world, peaks, e2e=False, keep_out=False):
+    """One workload of the batched entry points (anchored or dense mask), forward
+    or backward.  Returns the measurement as a dict."""
+    import torch
+    dense = mode == "dense"
+    dt = "bf16" if d["dtype"] == "bf16" else "fp32"
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    esize = 2 if dt == "bf16" else 4
+    B, Q, H, S, bs = d["B"], d["Q"], d["H"], d["S"], d["block_size"]
+    dn, dr, dv = d["d_nope"], d["d_rope"], d["d_v"]
+    work = metrics.anchored_work(d["anchors"], S, Q, H, bs, dn, dr, dv, esize=esize)
+    if dense:  # the mask is read once more; visibility is the same as the anchored rule's
+        work["bytes"] += B * Q * (S + Q) * esize - d["anchors"].size * 4
+    host = {k: d[k] for k in ("q", "k_nope", "k_rope", "v")}
+    dev = {k: to_dev(v, dt, device) for k, v in host.items()}
+    anchors = torch.from_numpy(d["anchors"]).to(device)
+    out = torch.empty((B, Q, H, dv), dtype=tdt, device=device)
+    lse = torch.empty((B, H, Q), dtype=torch.float32, device=device) if (keep_out or backward) else None
+    mode_code = dfl.MODE_DENSE if dense else dfl.MODE_ANCHORED
+    code = dfl.DFLASH_BF16 if dt == "bf16" else dfl.DFLASH_FP32
+    ws = torch.empty(max(dfl.dflash_attn_workspace_size(mode_code, B, H, S, Q, dn, dr, dv, code), 1),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 256 MiB > 129 MB L2
+    mask = None
+    if dense:  # the additive block mask, built on the device from the anchors (+ padding columns)
+        mask = dfl.dflash_build_mask(anchors, bs, S, dtype=tdt)
+        if d.get("pad"):
+            mask[:, :, :, S - d["pad"]:S] = float("-inf")
 
-        # A serving loop overlaps transfers with compute: the inputs of step k+1
-        # travel host->device and the output of step k-1 device->host while step k
-        # computes (two device buffer sets; one stream per direction).  Every step
-        # still copies all of its inputs in and its whole output out.
-        bufs = []
-        for _ in range(2):
-            bset = {k: torch.empty_like(t) for k, t in dev.items()}
-            bset["anchors"] = torch.empty_like(anchors)
-            bset["out"] = torch.empty_like(out)
-            bufs.append(bset)
-        outs_h = [out_h, torch.empty_like(out_h).pin_memory()]
-        h2d_stream, d2h_stream = torch.cuda.Stream(device), torch.cuda.Stream(device)
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_done = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
+    def fwd(o=out, l=lse):
+        if dense:
+            dfl.dflash_attn_dense(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], mask, out=o, lse=l,
+                                  workspace=ws, stream=stream)
+        else:
+            dfl.dflash_attn_anchored(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], anchors, bs, out=o, lse=l,
+                                     workspace=ws, stream=stream)
 
-        def e2e_steps(n):
-            for k in range(n):
-                bi = k % 2
-                bset = bufs[bi]
-                with torch.cuda.stream(h2d_stream):
-                    if k >= 2:
-                        h2d_stream.wait_event(ev_out[bi])  # step k-2 has computed and left
-                    for name, t in pinned.items():
-                        bset[name].copy_(t, non_blocking=True)
-                    bset["anchors"].copy_(an_h, non_blocking=True)
-                    ev_in[bi].record(h2d_stream)
-                stream.wait_event(ev_in[bi])
-                dfl.dflash_attn_anchored(bset["q"], bset["k_nope"], bset["k_rope"], bset["v"], bset["anchors"], bs,
-                                         out=bset["out"], workspace=ws, stream=stream)
-                ev_done[bi].record(stream)
-                with torch.cuda.stream(d2h_stream):
-                    d2h_stream.wait_event(ev_done[bi])
-                    outs_h[bi].copy_(bset["out"], non_blocking=True)
-                    ev_out[bi].record(d2h_stream)
-
-        e2e_steps(4)
-        torch.cuda.synchronize(device)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(h2d_stream)
-        e2e_steps(args.steps)
-        h2d_stream.wait_stream(d2h_stream)
-        h2d_stream.wait_stream(stream)
-        e1.record(h2d_stream)
-        torch.cuda.synchronize(device)
-        e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
-        e2e = {"value": job_value(work["flops"], world, e_ms) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms,
-               "overlap": "inputs of step k+1 in and output of step k-1 out while step k computes "
-                          "(two device buffer sets, one stream per direction)"}
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and headline:
-        # The whole workload (every query row, every head), repeated until about
-        # 10 s of oracle time has accumulated.
-        rows = np.arange(0, B * Q, dtype=np.int64)
-        total_t, total_f, reps, threads = 0.0, 0, 0, 1
-        while reps == 0 or total_t < 10.0:
-            dt, fl, threads = time_oracle(d, rows)
-            total_t += dt
-            total_f += fl
-            reps += 1
-        cpu = {"value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"the whole {WORKLOAD} workload ({rows.size} rows x {H} heads, {fl / 1e9:.1f} GFLOP "
-                         f"unmasked) x {reps}, {total_t:.1f} s"}
-
-    metric = METRIC
+    step, kernel = fwd, ("mask scan + attention" if dense else "attention (one launch per step)")
     if backward:
-        metric = ("DFlash block-attn backward TFLOP/s (unmasked FLOPs, 2*(3*d_qk+2*d_v) per visible pair) "
-                  "& % of GB300 bf16 roofline")
-    line = {"metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_desc(d) + (" (dense mask entry point)" if dense else "")
-                       + (" backward (dq, dk_nope, dk_rope, dv)" if backward else ""),
-                       "l2": "flushed between timed steps (256 MiB write)",
-                       "unmasked_flops_per_step": work["flops"], "algorithmic_bytes_per_step": work["bytes"],
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": traffic if headline else None,
-                         "peak_source": f"bf16_tflops ({peak_src})",
-                         "kernel": ("prep + dq + dk/dv + rope finish" + (" (+ mask scan)" if dense else ""))
-                         if backward else ("mask scan + attention" if dense else "attention (one launch per step)")},
-            "pct_bf16_roofline": 100.0 * achieved / peak,
-            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": int(launches), "clocks": clocks.summary()}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    return 0
+        # The backward step takes the forward's out and lse (computed here, once,
+        # outside the timed region) and the output gradient dout.
+        fwd()
+        dout = to_dev(synth.make_dout(d), dt, device)
+        grads = tuple(torch.empty_like(dev[k]) for k in ("q", "k_nope", "k_rope", "v"))
+        bmode = dfl.MODE_DENSE_BACKWARD if dense else dfl.MODE_ANCHORED_BACKWARD
+        bws = torch.empty(dfl.dflash_attn_workspace_size(bmode, B, H, S, Q, dn, dr, dv, code), dtype=torch.uint8,
+                          device=device)
+        work = dict(work, flops=work["flops"] // metrics.flops_per_pair(dn, dr, dv)
+                    * metrics.backward_flops_per_pair(dn, dr, dv))
+        kernel = "prep + dq + dk/dv + rope finish" + (" (+ mask scan)" if dense else "")
+
+        def step():
+            if dense:
+                dfl.dflash_attn_dense_backward(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], mask, out, lse,
+                                               dout, grads=grads, workspace=bws, stream=stream)
+            else:
+                dfl.dflash_attn_anchored_backward(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], anchors, bs,
+                                                  out, lse, dout, grads=grads, workspace=bws, stream=stream)
+
+    times, launches, clocks = timed_loop(step, steps, warmup, device, stream, flush, world, dfl)
+    kernel_ms = sum(times) / len(times)
+    ms = max_over_ranks(kernel_ms, world, device)
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = work["flops"] / (kernel_ms / 1e3) / 1e12
+    res = {"workload": workload_desc(d, mode) + (" backward (dq, dk_nope, dk_rope, dv)" if backward else ""),
+           "value": job_value(work["flops"], world, ms) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+           "steps": steps, "unmasked_flops_per_step": work["flops"], "algorithmic_bytes_per_step": work["bytes"],
+           "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak, "frac_of_sustained": achieved / sustained, "kernel": kernel},
+           "gpu_launches": launches, "clocks": clocks}
+    if dt == "bf16" and not backward:
+        res["target"] = {"frac": TARGET_FRAC["tensor"], "met": bool(achieved / peak >= TARGET_FRAC["tensor"])}
+    if keep_out:
+        fwd()
+        torch.cuda.synchronize(device)
+        res["_out"] = out.double().cpu().numpy()
+        res["_lse"] = lse.double().cpu().numpy()
+    if e2e and not dense and not backward:
+        res["e2e"] = measure_e2e(dfl, d, dev, anchors, out, ws, stream, device, world, work, steps, dt)
+    return res
 
 
-def run_decode(args):
+def measure_e2e(dfl, d, dev, anchors, out, ws, stream, device, world, work, steps, dt):
+    """The same metric end to end through the public API from pinned host
+    buffers: every step copies its inputs host->device and its output back."""
+    import torch
+    bs = d["block_size"]
+    host = {k: np.ascontiguousarray(d[k]) for k in ("q", "k_nope", "k_rope", "v")}
+    if dt == "bf16":
+        pinned = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory() for k, v in host.items()}
+    else:
+        pinned = {k: torch.from_numpy(v).pin_memory() for k, v in host.items()}
+    an_h = torch.from_numpy(d["anchors"]).pin_memory()
+    out_h = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values()) + an_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size()
+
+    # A serving loop overlaps transfers with compute: the inputs of step k+1
+    # travel host->device and the output of step k-1 device->host while step k
+    # computes (two device buffer sets; one stream per direction).  Every step
+    # still copies all of its inputs in and its whole output out.
+    bufs = []
+    for _ in range(2):
+        bset = {k: torch.empty_like(t) for k, t in dev.items()}
+        bset["anchors"] = torch.empty_like(anchors)
+        bset["out"] = torch.empty_like(out)
+        bufs.append(bset)
+    outs_h = [out_h, torch.empty_like(out_h).pin_memory()]
+    h2d_stream, d2h_stream = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_steps(n):
+        for k in range(n):
+            bi = k % 2
+            bset = bufs[bi]
+            with torch.cuda.stream(h2d_stream):
+                if k >= 2:
+                    h2d_stream.wait_event(ev_out[bi])  # step k-2 has computed and left
+                for name, t in pinned.items():
+                    bset[name].copy_(t, non_blocking=True)
+                bset["anchors"].copy_(an_h, non_blocking=True)
+                ev_in[bi].record(h2d_stream)
+            stream.wait_event(ev_in[bi])
+            dfl.dflash_attn_anchored(bset["q"], bset["k_nope"], bset["k_rope"], bset["v"], bset["anchors"], bs,
+                                     out=bset["out"], workspace=ws, stream=stream)
+            ev_done[bi].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(ev_done[bi])
+                outs_h[bi].copy_(bset["out"], non_blocking=True)
+                ev_out[bi].record(d2h_stream)
+
+    e2e_steps(4)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(h2d_stream)
+    e2e_steps(steps)
+    h2d_stream.wait_stream(d2h_stream)
+    h2d_stream.wait_stream(stream)
+    e1.record(h2d_stream)
+    torch.cuda.synchronize(device)
+    e_ms = max_over_ranks(e0.elapsed_time(e1) / steps, world, device)
+    return {"value": job_value(work["flops"], world, e_ms) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms,
+            "overlap": "inputs of step k+1 in and output of step k-1 out while step k computes "
+                       "(two device buffer sets, one stream per direction)"}
+
+
+def measure_decode(dfl, steps, warmup, device, world, peaks, requests=None):
     """The ragged decode workload: 64 requests x 16 draft rows, contexts
     log-uniform in [1024, 32768], H=32.  HBM-bound: the roofline is bytes."""
     import torch
-    torch.cuda.set_device(0)
-    device = torch.device("cuda", 0)
-    import dflash_block_draft_gb300 as dfl
-    dfl.load_library()
-    d = synth.make("decode_bf16", **({"R": args.requests} if args.requests else {}))
+    d = synth.make("decode_bf16", **({"R": requests} if requests else {}))
     H, bs = d["H"], d["block_size"]
     work = metrics.ragged_work(d["q_offsets"], d["kv_offsets"], d["anchors"], H, bs, d["d_nope"], d["d_rope"],
                                d["d_v"])
@@ -479,43 +558,112 @@ def run_decode(args):
         dfl.dflash_attn_ragged(dev["q"], dev["k_nope"], dev["k_rope"], dev["v"], qo, ko, an, bs, 16, out=out,
                                workspace=ws, stream=stream)
 
-    for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize(device)
-    if dfl.dflash_last_device_error() != 0:
-        raise RuntimeError("device error during warm-up")
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clocks = ClockSampler(0)
-    launches0 = dfl.dflash_kernel_launches()
-    torch.cuda.synchronize(device)
-    clocks.start()
-    for k in range(args.steps):
-        flush.zero_()
-        ev[k][0].record(stream)
-        step()
-        ev[k][1].record(stream)
-    torch.cuda.synchronize(device)
-    clocks.stop()
-    launches = dfl.dflash_kernel_launches() - launches0
-    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    peaks, src = load_peaks()
-    gbs = work["bytes"] / (ms / 1e3) / 1e9
+    times, launches, clocks = timed_loop(step, steps, warmup, device, stream, flush, world, dfl)
+    kernel_ms = sum(times) / len(times)
+    ms = max_over_ranks(kernel_ms, world, device)
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    line = {"metric": "DFlash block-attn ragged decode: algorithmic HBM GB/s (and unmasked TFLOP/s)",
-            "value": gbs, "unit": "GB/s", "tflops": work["flops"] / (ms / 1e3) / 1e12, "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"decode_bf16: R={d['R']} x 16 rows, H={H}, contexts log-uniform [1024,32768], "
-                                   f"total_kv={d['total_kv']}", "l2": "flushed between timed steps (256 MiB write)",
-                       "algorithmic_bytes_per_step": work["bytes"], "unmasked_flops_per_step": work["flops"]},
+    gbs = work["bytes"] / (kernel_ms / 1e3) / 1e9
+    return {"workload": workload_desc(d), "value": job_value(work["bytes"], world, ms) / 1e9, "unit": "GB/s",
+            "tflops": work["flops"] / (kernel_ms / 1e3) / 1e12, "ms_per_step": ms, "steps": steps,
+            "algorithmic_bytes_per_step": work["bytes"], "unmasked_flops_per_step": work["flops"],
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                         "traffic": load_traffic("decode_bf16", work["bytes"]), "peak_source": f"hbm_gbs ({src})",
+                         "traffic": load_traffic("decode_bf16", work["bytes"]),
                          "kernel": "plan + split attention + combine (one step; the attention kernel is 95 % of it)",
                          "traffic_note": "attn_decode_kernel DRAM bytes from a 16-request capture, scaled by "
                                          "algorithmic bytes"},
-            "gpu_launches": int(launches), "clocks": clocks.summary()}
-    print(json.dumps(line), flush=True)
+            "target": {"frac": TARGET_FRAC["hbm"], "met": bool(gbs / peak >= TARGET_FRAC["hbm"])},
+            "gpu_launches": launches, "clocks": clocks}
+
+
+def release_memory():
+    import gc
+
+    import torch
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    import dflash_block_draft_gb300 as dfl
+    dfl.load_library()
+    peaks, peak_src = load_peaks()
+    backward = args.pass_ == "backward"
+
+    if args.workload == "decode_bf16":
+        head = measure_decode(dfl, args.steps, args.warmup, device, world, peaks, args.requests)
+        metric = "DFlash block-attn ragged decode: algorithmic HBM GB/s (and unmasked TFLOP/s)"
+        d_head = None
+        head["roofline"]["peak_source"] = f"hbm_gbs ({peak_src})"
+    else:
+        d_head = synth.make(args.workload, **({"H": args.heads} if args.heads else {}))
+        head = measure_batched(dfl, d_head, args.mode, backward, args.steps, args.warmup, device, world, peaks,
+                               e2e=not args.no_e2e)
+        metric = METRIC
+        if backward:
+            metric = ("DFlash block-attn backward TFLOP/s (unmasked FLOPs, 2*(3*d_qk+2*d_v) per visible pair) "
+                      "& % of GB300 bf16 roofline")
+        head["roofline"]["peak_source"] = f"bf16_tflops ({peak_src}); frac_of_sustained against bf16_tflops_sustained"
+        key = args.workload if args.mode == "anchored" else f"{args.workload}:dense"
+        head["roofline"]["traffic"] = None if backward else load_traffic(key)
+    release_memory()
+
+    headline = args.workload == WORKLOAD and args.mode == "anchored" and not backward and not args.heads
+    per_config, tiny = None, None
+    if headline and world == 1 and not args.no_per_config:
+        per_config = {}
+        for w, mode in PER_CONFIG:
+            if w == "decode_bf16":
+                r = measure_decode(dfl, args.steps, args.warmup, device, 1, peaks)
+            else:
+                dw = synth.make(w)
+                r = measure_batched(dfl, dw, mode, False, args.steps, args.warmup, device, 1, peaks,
+                                    keep_out=w == "tiny_fp32")
+                if w == "tiny_fp32":
+                    tiny = {"inputs": dw, "out": r.pop("_out"), "lse": r.pop("_lse")}
+                    r["roofline"] = {"bound": "none (parity only)", "note": "fp32 exactness path (CUDA cores)"}
+                    r.pop("target", None)
+                else:
+                    key = w if mode == "anchored" else f"{w}:dense"
+                    r["roofline"]["traffic"] = load_traffic(key)
+                del dw
+            per_config[f"{w}:{mode}"] = r
+            release_memory()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and headline:
+        cpu, parity = cpu_baseline_leg(d_head, tiny)
+        if parity is not None and per_config is not None:
+            per_config["tiny_fp32:anchored"]["parity"] = parity
+
+    line = {"metric": metric, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": head["workload"], "l2": "flushed between timed steps (256 MiB write)",
+                       "unmasked_flops_per_step": head["unmasked_flops_per_step"],
+                       "algorithmic_bytes_per_step": head["algorithmic_bytes_per_step"],
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": head["roofline"],
+            "e2e": head.get("e2e"), "cpu_baseline": cpu, "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"]}
+    if head["roofline"]["unit"] == "TFLOP/s":
+        line["pct_bf16_roofline"] = 100.0 * head["roofline"]["frac"]
+    if "target" in head:
+        line["target"] = head["target"]
+    if per_config is not None:
+        line["per_config"] = per_config
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
     return 0
 
 
@@ -548,20 +696,25 @@ def load_traffic(key=None, alg_bytes=None):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["prefill_bf16", "training_bf16", "long_bf16", "decode_bf16"],
-                    default="prefill_bf16",
-                    help="prefill_bf16 is the headline; the others are the remaining bf16 workloads "
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure the headline workload only (no per_config block)")
+    ap.add_argument("--workload", choices=["long_bf16", "prefill_bf16", "training_bf16", "decode_bf16", "tiny_fp32"],
+                    default=WORKLOAD,
+                    help="long_bf16 (the largest workload) is the headline; the others are the rest of the suite "
                          "(decode_bf16 is HBM-bound and reported in GB/s)")
     ap.add_argument("--mode", choices=["anchored", "dense"], default="anchored",
                     help="entry point for the batched workloads")
     ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
                     help="batched workloads: time the forward call, or the backward call (gradients of "
                          "q, k_nope, k_rope, v) given the forward's out and lse")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="batched workloads only: use this many heads instead of the workload's (same recipe "
+                         "otherwise; for profiling captures that must stay small)")
     ap.add_argument("--requests", type=int, default=None,
                     help="decode_bf16 only: draw this many requests instead of 64 (same recipe; "
                          "for profiling captures that must stay small)")
@@ -570,8 +723,6 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
-    if args.workload == "decode_bf16":
-        return run_decode(args)
     return run_ours(args)
 
 
