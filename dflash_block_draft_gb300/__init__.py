@@ -36,7 +36,7 @@ STATUS = {0: "DFLASH_OK", 1: "DFLASH_ERR_INVALID", 2: "DFLASH_ERR_SHAPE", 3: "DF
 EXPORTS = ("dflash_attn_dense", "dflash_attn_anchored", "dflash_attn_ragged", "dflash_attn_workspace_size",
            "dflash_build_schedule_host", "dflash_scan_mask", "dflash_status_string", "dflash_last_device_error",
            "dflash_kernel_launches", "dflash_attn_dense_noalloc", "dflash_build_mask",
-           "dflash_attn_anchored_backward", "dflash_attn_dense_backward")
+           "dflash_attn_anchored_backward", "dflash_attn_dense_backward", "dflash_test_inject_stall")
 
 
 class DFlashError(RuntimeError):
@@ -86,6 +86,8 @@ def load_library(path: str | None = None):
         lib.dflash_attn_dense_backward.argtypes = [DP, I, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P]
         lib.dflash_attn_anchored_backward.restype = ctypes.c_int
         lib.dflash_attn_dense_backward.restype = ctypes.c_int
+        lib.dflash_test_inject_stall.argtypes = [ctypes.c_ulonglong, I]
+        lib.dflash_test_inject_stall.restype = None
         lib.dflash_kernel_launches.argtypes = []
         lib.dflash_kernel_launches.restype = ctypes.c_uint64
         for name in ("dflash_attn_dense", "dflash_attn_anchored", "dflash_attn_ragged",
@@ -386,3 +388,10 @@ def dflash_kernel_launches() -> int:
 def dflash_last_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error word."""
     return int(load_library().dflash_last_device_error(_stream(stream)))
+
+
+def dflash_test_inject_stall(wait_budget_ns: int = 0, stall_cta: int = -1) -> None:
+    """Test export: set the bounded-wait budget (0 = the 2 s default) and the CTA
+    whose producer leaves its first work item's key tiles unloaded (-1 = none),
+    for every later forward call in this process."""
+    load_library().dflash_test_inject_stall(int(wait_budget_ns), int(stall_cta))

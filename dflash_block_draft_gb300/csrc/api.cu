@@ -19,6 +19,10 @@ __device__ unsigned g_error_word;
 
 namespace {
 std::atomic<uint64_t> g_launches{0};
+// Test fault injection (dflash_test_inject_stall): wait budget and stalled CTA.
+std::atomic<unsigned long long> g_wait_ns{0};
+std::atomic<int> g_stall_cta{-1};
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 }
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
@@ -165,6 +169,9 @@ AttnParams base_params(int H, int dn, int dr, int dv, float scale, const void* q
   p.scale = resolve_scale(scale, dn, dr);
   p.scale_log2 = (float)((double)p.scale * 1.4426950408889634);
   p.err = error_word();
+  const unsigned long long w = g_wait_ns.load(std::memory_order_relaxed);
+  p.wait_ns = w ? w : kDefaultWaitNs;
+  p.stall_cta = g_stall_cta.load(std::memory_order_relaxed);
   return p;
 }
 
@@ -179,21 +186,8 @@ bool use_tc(dflash_dtype_t dtype, int dn, int dr, int dv, long long q_rows, long
   return !env_flag("DFLASH_FORCE_SIMT");
 }
 
-// Two tensor-core kernels compute the same result.  attn_tc.cu (one CTA per
-// item of two query tiles) is the default: measured on GB300 it is the faster
-// of the two on every bf16 workload (anchored, S+Q = 8192 / 16384 / 34816:
-// by 13 %, 10 % and 5 %; dense by more).  attn_tc2.cu (CTA pairs, items of
-// four query tiles, tcgen05 pair MMAs) alternates the two halves of an item on
-// the tensor pipe, but its pair QK runs at about half the per-SM MMA rate and
-// its larger items carry more masked work.  DFLASH_TC_KERNEL=2 selects it
-// (DFLASH_TC_KERNEL=1 the default kernel).
 cudaError_t launch_tc(const AttnParams& p, int segments, int nqt, long long q_rows, long long kv_rows,
                       cudaStream_t stream) {
-  const char* force = getenv("DFLASH_TC_KERNEL");
-  bool pair = false;
-  if (force && force[0] == '1') pair = false;
-  if (force && force[0] == '2') pair = true;
-  if (pair) return launch_attn_tc2(p, segments, nqt, q_rows, kv_rows, stream);
   return launch_attn_tc(p, segments, nqt, q_rows, kv_rows, stream);
 }
 
@@ -373,6 +367,7 @@ dflash_status_t dflash_attn_ragged(int R, int H, int d_nope, int d_rope, int d_v
   p.R = R;
   p.total_q = total_q;
   p.total_kv = total_kv;
+  p.max_q = max_q_len;
   p.q_off = q_offsets;
   p.kv_off = kv_offsets;
   p.anchors = anchors;
@@ -474,6 +469,11 @@ dflash_status_t dflash_attn_dense_backward(const dflash_dims_t* dims, dflash_dty
 }
 
 uint64_t dflash_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void dflash_test_inject_stall(unsigned long long wait_budget_ns, int stall_cta) {
+  g_wait_ns.store(wait_budget_ns, std::memory_order_relaxed);
+  g_stall_cta.store(stall_cta < 0 ? -1 : stall_cta, std::memory_order_relaxed);
+}
 
 dflash_status_t dflash_last_device_error(dflash_stream_t stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DFLASH_ERR_CUDA;

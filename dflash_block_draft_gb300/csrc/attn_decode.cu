@@ -31,6 +31,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace dflash {
 namespace {
@@ -71,8 +72,8 @@ constexpr uint32_t kTmemCols = 64;
 constexpr uint32_t kColS = 0, kColO = 32;  // S^T buffers at 0 and 16
 
 constexpr int kThreads = 192;
-constexpr uint64_t kWaitBudgetNs = 2000000000ull;
-constexpr uint32_t kSleepHintNs = 100000;
+using tc::Ctl;
+using tc::kWaitBudgetNs;
 constexpr uint32_t kSoftmaxBarrier = 1;  // named barrier of the 4 softmax warps
 
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, kQN, 0, 0);  // K and Q both K-major
@@ -136,27 +137,6 @@ __device__ __forceinline__ int next_tile(const DecodeArgs& a, const Unit& it, in
   return it.kt1;
 }
 
-struct Ctl {
-  uint32_t bar0;
-  volatile int* abort;
-  unsigned* err;
-  __device__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
-  __device__ bool wait(int i, uint32_t parity) const {
-    const uint32_t b = bar(i);
-    if (ptx::mbar_try_wait(b, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer();
-    for (;;) {
-      if (ptx::mbar_try_wait_sleep(b, parity, kSleepHintNs)) return true;
-      if (*abort) return false;
-      if (ptx::globaltimer() - t0 > kWaitBudgetNs) {
-        *abort = 1;
-        record_error(err, DFLASH_ERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-};
-
 __global__ void __launch_bounds__(kThreads, 1)
     attn_decode_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmKn, const __grid_constant__ CUtensorMap tmKr,
@@ -172,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ctl.bar0 = sbase + kOffBar;
   ctl.abort = reinterpret_cast<volatile int*>(smem + kOffAbort);
   ctl.err = p.err;
+  ctl.budget = p.wait_ns;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
   float* red = reinterpret_cast<float*>(smem + kOffRed);  // [4][kQN] per-warp values
   unsigned* vote = reinterpret_cast<unsigned*>(red + 4 * kQN);  // [3] vote words, used in rotation
@@ -226,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tma_load_3d(sbase + kOffQ + pn * kQPanel, &tmQ, ctl.bar(BAR_Q_FULL), 64 * pn, it.h,
                            (int)it.sg.q0);
         ++n;
+        if ((int)blockIdx.x == p.stall_cta) break;  // timeout test: this unit's key tiles never arrive
         for (int kt = next_tile(a, it, it.kt0 - 1); kt < it.kt1 && !stop; kt = next_tile(a, it, kt)) {
           const int krow = (int)(it.sg.kv0 + (long long)kt * kBN);
           for (uint32_t pn = 0; pn < kPanelsPerTile; ++pn, ++pc) {
@@ -243,6 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // Wind-down (also after a timeout): the loads still outstanding -- at most
+      // the last kRing panels and the last Q tile -- land before the CTA exits.
+      for (uint32_t i = pc > kRing ? pc - kRing : 0u; i < pc; ++i)
+        ctl.wait_landed(BAR_RING_FULL + i % kRing, (i / kRing) & 1u);
+      if (n > 0) ctl.wait_landed(BAR_Q_FULL, (n - 1) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer

@@ -19,8 +19,9 @@
 // Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM, warps 1
 // and 2 issue the MMAs of halves 0 and 1 (warp 3 idle), warps 4..7 and 8..11
 // are the softmax/epilogue warpgroups of halves 0 and 1.  The first warpgroup
-// gives registers back (setmaxnreg 120) so that the softmax warpgroups get 192
-// registers a thread: 128*120 + 256*192 = 384*168, the launch budget.  Each
+// gives registers back (setmaxnreg 104, or 120 for dense masks) so that the
+// softmax warpgroups get 200 (192) registers a thread: 128*104 + 256*200 =
+// 384*168, the launch budget.  Each
 // half's MMAs go out from its own thread in the order
 //   QK_i(j) [softmax_i(j)] PV_i(j) QK_i(j+1) ...
 // PV_i(j) goes out in two parts: keys 0-63 as soon as the softmax has written
@@ -31,7 +32,7 @@
 // two issue streams interleave MMA by MMA and both S land together.  Turns on
 // whole groups (PV and QK) would let one half's softmax overlap all of the
 // other half's MMAs, but then the ring must hold two key tiles per half, more
-// than fits (the CTA-pair kernel of attn_tc2.cu does that).
+// than fits next to the two Q tiles.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
 // P_i (bf16 pairs) overwrites the first 64 columns of S_i once they are read,
 // and QK_i(j+1) is issued only after PV_i(j), which the tensor pipe runs in order.
@@ -89,8 +90,13 @@ constexpr uint32_t kColS = 0, kColO = 256;  // S_i at kColS + 128 i, O_i at kCol
 
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
-constexpr uint32_t kCtlRegs = 120, kSoftmaxRegs = 192;
-static_assert(128 * kCtlRegs + 256 * kSoftmaxRegs == kThreads * kLaunchRegs, "register split");
+// Register split per mask kind (the anchored softmax keeps more per-row state;
+// the dense control warps decode more per item): no spills either way.
+template <bool DENSE>
+struct RegSplit {
+  static constexpr uint32_t ctl = DENSE ? 120 : 104, softmax = DENSE ? 192 : 200;
+  static_assert(128 * ctl + 256 * softmax == kThreads * kLaunchRegs, "register split");
+};
 using tc::kWaitBudgetNs;
 using tc::Ctl;
 using tc::PrepCtx;
@@ -238,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ctl.bar0 = sbase + kOffBar;
   ctl.abort = reinterpret_cast<volatile int*>(smem + kOffAbort);
   ctl.err = p.err;
+  ctl.budget = p.wait_ns;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
 
   if (threadIdx.x == 0) {
@@ -275,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t ring = sbase + kOffRing;
-  if (warp < 4) ptx::setmaxnreg_dec<kCtlRegs>();
+  if (warp < 4) ptx::setmaxnreg_dec<RegSplit<DENSE>::ctl>();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -296,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              qrow);
         }
         ++n_items;
+        if ((int)blockIdx.x == p.stall_cta) break;  // timeout test: this item's key tiles never arrive
         for (int kt = next_tile<DENSE>(a, it, -1); kt < it.nkt && !stop; kt = next_tile<DENSE>(a, it, kt)) {
           const int krow = (int)(it.sg.kv0 + (long long)kt * kBN);
           const bool vf = v_first(pc / kPanelsPerTile);
@@ -316,6 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // Wind-down (also after a timeout): every load this thread issued lands
+      // before the CTA exits, since a copy still in flight would write into
+      // shared memory the CTA no longer owns.  The last kRing panels and the
+      // last Q load are the only ones that can still be outstanding.
+      for (uint32_t i = pc > kRing ? pc - kRing : 0u; i < pc; ++i)
+        ctl.wait_landed(BAR_RING_FULL + i % kRing, (i / kRing) & 1u);
+      if (n_items > 0) ctl.wait_landed(BAR_Q_FULL, (n_items - 1) & 1u);
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
@@ -443,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue (warps 4..11)
-    ptx::setmaxnreg_inc<kSoftmaxRegs>();
+    ptx::setmaxnreg_inc<RegSplit<DENSE>::softmax>();
     const int half = (warp - 4) >> 2;  // query tile of the pair
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // TMEM lane = query row within the tile
@@ -466,6 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = h_r0 + row;
       const bool row_ok = h_has && i < h_r1;
       const int S = it.sg.S, Qn = it.sg.Q, K = S + Qn;
+      // The row's output and lse addresses, resolved once (fewer live registers
+      // across the tile loop).
+      uint4* out_dst = row_ok ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                         ((it.sg.q0 + i) * p.H + it.h) * (long long)kDv)
+                              : nullptr;
+      float* lse_dst = row_ok && p.lse ? p.lse + it.sg.lse0 + (long long)it.h * it.sg.lse_hs + i : nullptr;
       int ctx_lim = 0, nlo = 0, nhi = 0;
       const __nv_bfloat16* mrow = nullptr;
       if (DENSE) {
@@ -509,7 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::prefetch_l1(mp + min(128, span - 1));
           ptx::prefetch_l1(mp + span - 1);
         }
-        if (!ctl.wait(BAR_S_FULL + half, g & 1u)) {
+        // Waits feeding warp-collective TMEM accesses are made warp-uniform: a
+        // timeout seen by one lane stops the whole warp.
+        if (!__all_sync(0xffffffffu, ctl.wait(BAR_S_FULL + half, g & 1u))) {
           stop = true;
           break;
         }
@@ -536,29 +559,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_wait_ld();
           mask64(x, kind, 64 * hh, pc);
           const float mh = max64(x) * cm;
-          if (mh > m_used + 8.0f) {  // also when m is still -inf and this half sees a key
-            if (m_used != -INFINITY) {
-              const float alpha = ptx::ex2(m_used - mh);
-              // the second half: O may still be taking PV of keys 0-63 (P written
-              // with the old reference); scale O once that has completed
-              if (hh == 1 && !ctl.wait(BAR_PV_LO + half, g & 1u)) stop = true;
-              ptx::tc_fence_after();
+          const bool raise = mh > m_used + 8.0f;  // also when m is still -inf and this half sees a key
+          const bool scale_o = raise && m_used != -INFINITY;
+          // O is rescaled by whole warps (TMEM loads and stores are warp-collective):
+          // lanes whose reference did not move scale by 1.
+          if (__any_sync(0xffffffffu, scale_o)) {
+            const float alpha = scale_o ? ptx::ex2(m_used - mh) : 1.f;
+            // the second half: O may still be taking PV of keys 0-63 (P written
+            // with the old reference); scale O once that has completed
+            if (hh == 1 && !__all_sync(0xffffffffu, ctl.wait(BAR_PV_LO + half, g & 1u))) stop = true;
+            ptx::tc_fence_after();
 #pragma unroll 1
-              for (int cc = 0; cc < kDv; cc += 32) {
-                uint32_t o[32];
-                ptx::tmem_ld32(o_col + cc, o);
-                ptx::tmem_wait_ld();
+            for (int cc = 0; cc < kDv; cc += 32) {
+              uint32_t o[32];
+              ptx::tmem_ld32(o_col + cc, o);
+              ptx::tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                ptx::tmem_st32(o_col + cc, o);
-              }
-              ptx::tmem_wait_st();
-              l *= alpha;
-              lsum.x *= alpha;
-              lsum.y *= alpha;
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              ptx::tmem_st32(o_col + cc, o);
             }
-            m_used = mh;
+            ptx::tmem_wait_st();
+            l *= alpha;
+            lsum.x *= alpha;
+            lsum.y *= alpha;
           }
+          if (raise) m_used = mh;
           const float msub = m_used == -INFINITY ? 0.f : m_used;
           const float2 mul2 = make_float2(cm, cm), neg2 = make_float2(-msub, -msub);
           uint32_t pk[32];
@@ -589,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ob[kDv / 2];
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (any_tile) {
-        if (!ctl.wait(BAR_O_FULL + half, n_full & 1u)) break;
+        if (!__all_sync(0xffffffffu, ctl.wait(BAR_O_FULL + half, n_full & 1u))) break;
         ++n_full;
         ptx::tc_fence_after();
 #pragma unroll
@@ -606,8 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < kDv / 2; ++e) ob[e] = 0u;
       }
       if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                              ((it.sg.q0 + i) * p.H + it.h) * (long long)kDv);
+        uint4* dst = out_dst;
         if (a.out_v8) {
           // a row is 256 contiguous bytes: eight 32-byte stores (a sector each)
 #pragma unroll
@@ -616,9 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int v = 0; v < kDv / 8; ++v) dst[v] = make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]);
         }
-        if (p.lse)
-          p.lse[it.sg.lse0 + (long long)it.h * it.sg.lse_hs + i] =
-              l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        if (lse_dst) *lse_dst = l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
       }
     }
   }

@@ -36,12 +36,18 @@ struct AttnParams {
   const int32_t* anchors;
   // ragged
   int R, total_q, total_kv;
+  int max_q;  // the caller's bound on every request's q_len (kernels size their grids by it)
   const int32_t* q_off;
   const int32_t* kv_off;
   // dense tile classes [B, nqt, nkt] (uint8), produced by the mask scan
   const uint8_t* classes;
   int nqt, nkt;
   unsigned* err;  // device error word
+  // Bounded waits: the budget of one mbarrier wait, and (tests of the timeout
+  // path only; -1 otherwise) the CTA whose producer leaves its first work
+  // item's key tiles unloaded so that its consumers' waits run out.
+  unsigned long long wait_ns;
+  int stall_cta;
 };
 
 // One segment (batch row or request), resolved on the device.
@@ -67,7 +73,7 @@ __device__ __forceinline__ Seg resolve_segment(const AttnParams& p, int z) {
     const int k0 = p.kv_off[z], k1 = p.kv_off[z + 1];
     const int ql = q1 - q0, kl = k1 - k0;
     if (q0 < 0 || k0 < 0 || q1 > p.total_q || k1 > p.total_kv || ql < p.bs || ql % p.bs != 0 ||
-        q0 % p.bs != 0 || kl < ql) {
+        q0 % p.bs != 0 || kl < ql || ql > p.max_q) {
       s.ok = 0;
       record_error(p.err, DFLASH_ERR_INVALID);
       return s;

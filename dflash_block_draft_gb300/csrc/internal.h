@@ -58,9 +58,6 @@ int sm_count();
 bool tc_supported(int dn, int dr, int dv);
 cudaError_t launch_attn_tc(const AttnParams& p, int segments, int nqt, long long q_rows, long long kv_rows,
                            cudaStream_t stream);
-// The same operation on CTA pairs (attn_tc2.cu): items of four query tiles.
-cudaError_t launch_attn_tc2(const AttnParams& p, int segments, int nqt, long long q_rows, long long kv_rows,
-                            cudaStream_t stream);
 // Split-context decode path (ragged batches with at most 16 rows per request).
 bool decode_supported(int dn, int dr, int dv, int max_q_len);
 int decode_max_units(int R, int total_kv);

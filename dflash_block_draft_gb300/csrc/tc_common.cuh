@@ -1,6 +1,6 @@
-// tc_common.cuh -- device helpers shared by the tensor-core attention kernels
-// (attn_tc.cu, one CTA per item; attn_tc2.cu, a CTA pair per item): bounded
-// mbarrier waits and the per-row score preparation of the softmax.  Internal header.
+// tc_common.cuh -- device helpers of the tensor-core attention kernel
+// (attn_tc.cu): bounded mbarrier waits and the per-row score preparation of
+// the softmax.  Internal header.
 #pragma once
 
 #include <math.h>
@@ -11,18 +11,17 @@
 namespace dflash {
 namespace tc {
 
-constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s per wait unless the caller sets a budget
 constexpr uint32_t kSleepHintNs = 100000;           // re-check the budget every ~0.1 ms of sleep
 
 struct Ctl {
   uint32_t bar0;
   volatile int* abort;
   unsigned* err;
-  uint32_t peer_abort = 0;  // CTA pairs: the other CTA's abort flag (shared::cluster address)
+  uint64_t budget = kWaitBudgetNs;
   __device__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
   __device__ void give_up() const {
     *abort = 1;
-    if (peer_abort) ptx::st_cluster_u32(peer_abort, 1u);
     record_error(err, DFLASH_ERR_TIMEOUT);
   }
   // Bounded wait for the completion of the phase with parity `parity`.
@@ -34,23 +33,22 @@ struct Ctl {
       // sleep on the barrier (woken by the phase completing) rather than spin
       if (ptx::mbar_try_wait_sleep(b, parity, kSleepHintNs)) return true;
       if (*abort) return false;
-      if (ptx::globaltimer() - t0 > kWaitBudgetNs) {
+      if (ptx::globaltimer() - t0 > budget) {
         give_up();
         return false;
       }
     }
   }
-  // The same for a phase that arrivals from the other CTA of a pair complete.
-  __device__ bool wait_cluster(int i, uint32_t parity) const {
+  // Wind-down wait for a TMA load this thread issued: bulk copies of valid
+  // memory always land, so this ignores the abort flag; it is still bounded
+  // (kWaitBudgetNs) and records DFLASH_ERR_TIMEOUT if it ever runs out.
+  __device__ void wait_landed(int i, uint32_t parity) const {
     const uint32_t b = bar(i);
-    if (ptx::mbar_try_wait_cluster(b, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
-    for (;;) {
-      if (ptx::mbar_try_wait_sleep_cluster(b, parity, kSleepHintNs)) return true;
-      if (*abort) return false;
+    while (!ptx::mbar_try_wait_sleep(b, parity, kSleepHintNs)) {
       if (ptx::globaltimer() - t0 > kWaitBudgetNs) {
-        give_up();
-        return false;
+        record_error(err, DFLASH_ERR_TIMEOUT);
+        return;
       }
     }
   }

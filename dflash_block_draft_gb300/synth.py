@@ -48,6 +48,9 @@ class Workload:
     R: int = 0
     ctx_lo: int = 0
     ctx_hi: int = 0
+    # ragged only: when set, request r has nb_r blocks drawn uniformly from these
+    # counts (instead of nb each), and its anchors are drawn inside its context
+    q_blocks: tuple = ()
 
     @property
     def Q(self) -> int:
@@ -137,9 +140,10 @@ def make(w: Workload | str, seed: int | None = None, **override) -> dict:
     recipe).  Returns a dict of numpy arrays plus the integer dims.
     Batched: q [B,Q,H,dn+dr], k_nope [B,S+Q,H,dn], k_rope [B,S+Q,dr],
     v [B,S+Q,H,dv], anchors [B,nb] int32.
-    Ragged: q [R*q_len,H,dqk], k_nope [total_kv,H,dn], k_rope [total_kv,dr],
-    v [total_kv,H,dv], q_offsets/kv_offsets [R+1] int32, anchors [R*nb] int32
-    (each request's anchor equals its context length).
+    Ragged: q [total_q,H,dqk], k_nope [total_kv,H,dn], k_rope [total_kv,dr],
+    v [total_kv,H,dv], q_offsets/kv_offsets [R+1] int32, anchors [total_q/bs]
+    int32 (each request's anchors equal its context length; with q_blocks, the
+    requests' block counts differ and their anchors lie inside their contexts).
     """
     if isinstance(w, str):
         w = WORKLOADS[w]
@@ -153,12 +157,24 @@ def make(w: Workload | str, seed: int | None = None, **override) -> dict:
     if w.ragged:
         lo, hi = math.log(w.ctx_lo), math.log(w.ctx_hi)
         ctx = np.rint(np.exp(rng.uniform(lo, hi, size=w.R))).astype(np.int64)
-        q_len = w.nb * w.block_size
-        q_off = np.arange(w.R + 1, dtype=np.int64) * q_len
-        kv_off = np.concatenate([[0], np.cumsum(ctx + q_len)])
+        if w.q_blocks:
+            # Mixed draft lengths: nb_r blocks per request; anchors sorted uniform
+            # in [0, ctx_r], the last block's anchor the whole context.
+            nbr = rng.choice(np.asarray(w.q_blocks, np.int64), size=w.R)
+            q_lens = nbr * w.block_size
+            anchors = []
+            for r in range(w.R):
+                a = np.sort(rng.integers(0, ctx[r] + 1, size=nbr[r]))
+                a[-1] = ctx[r]
+                anchors.append(a)
+            anchors = np.concatenate(anchors).astype(np.int32)
+        else:
+            q_lens = np.full(w.R, w.nb * w.block_size, np.int64)
+            # One block per request in the decode shape: its anchor is its context length.
+            anchors = np.repeat(ctx, w.nb).astype(np.int32)
+        q_off = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int64)
+        kv_off = np.concatenate([[0], np.cumsum(ctx + q_lens)])
         total_q, total_kv = int(q_off[-1]), int(kv_off[-1])
-        # One block per request in the decode shape: its anchor is its context length.
-        anchors = np.repeat(ctx, w.nb).astype(np.int32)
         d.update(R=w.R, q_offsets=q_off.astype(np.int32), kv_offsets=kv_off.astype(np.int32),
                  anchors=anchors, context_lens=ctx.astype(np.int32), total_q=total_q, total_kv=total_kv,
                  q=_normal(seed, 0, (total_q, w.H, dqk), w.dtype),

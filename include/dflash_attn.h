@@ -146,8 +146,9 @@ DFLASH_API dflash_status_t dflash_attn_anchored(const dflash_dims_t* dims, dflas
  *   lse [H, total_q] fp32 (optional), offsets int32 [R+1] on the device.
  *   total_q, total_kv: extents of the packed tensors (q_offsets[R],
  *   kv_offsets[R]); max_q_len: an upper bound on every request's q_len.
- * Offsets that break these rules are recorded as DFLASH_ERR_INVALID in the
- * device error word and the offending request is skipped.
+ * Offsets that break these rules, and a request whose q_len exceeds
+ * max_q_len, are recorded as DFLASH_ERR_INVALID in the device error word and
+ * the offending request is skipped (its out and lse rows are not written).
  * Decode-shaped batches (small q_len, long context) are split along the
  * context and merged with a log-sum-exp combine kernel.
  */
@@ -286,6 +287,23 @@ DFLASH_API uint64_t dflash_kernel_launches(void);
  */
 DFLASH_API dflash_status_t dflash_build_mask(int B, int S, int Q, const int32_t* anchors, int nb, int block_size,
                                              dflash_dtype_t dtype, void* mask, dflash_stream_t stream);
+
+/*
+ * Test export: fault injection for the bounded-wait path.  Every mbarrier wait
+ * of the forward kernels (tensor-core and split-context decode) gives up after
+ * a budget -- 2 s unless set here -- records DFLASH_ERR_TIMEOUT in the device
+ * error word, and the CTA winds down: its issued TMA loads land, its issued
+ * MMAs complete, its TMEM is freed, and it returns; the context stays usable.
+ * This call sets, process-wide and for every later forward call until it is
+ * called again:
+ *   wait_budget_ns  budget of one wait (0 restores the 2 s default);
+ *   stall_cta       the CTA whose TMA producer leaves its first work item's
+ *                   key tiles unloaded, so that the waits on them run out
+ *                   (-1: none).  Other CTAs compute normally; the stalled
+ *                   CTA's output rows are left unwritten.
+ * Not for production use; not synchronised with calls in flight.
+ */
+DFLASH_API void dflash_test_inject_stall(unsigned long long wait_budget_ns, int stall_cta);
 
 /* Human-readable name of a status code (static storage). */
 DFLASH_API const char* dflash_status_string(dflash_status_t status);

@@ -257,21 +257,54 @@ def test_dense_from_anchors_with_padding_equals_anchored():
     np.testing.assert_allclose(ld, la, atol=TOL, rtol=0)
 
 
-def test_ragged_equals_per_request_loop():
-    d = synth.make("decode_bf16", R=5, H=2, d_nope=8, d_rope=4, d_v=6, ctx_lo=3, ctx_hi=40, block_size=4,
-                   nb=2)
+@pytest.mark.parametrize("q_blocks", [(), (1, 2, 3)], ids=["uniform", "mixed"])
+def test_ragged_equals_per_request_loop(q_blocks):
+    """Ragged == a B=1 anchored call per request on that request's slices.  With
+    mixed draft lengths a request's first global block q_offsets[r]/bs differs
+    from r*nb, so a mistake in how anchors are indexed across requests fails."""
+    R = 9 if q_blocks else 5
+    d = synth.make("decode_bf16", R=R, H=2, d_nope=8, d_rope=4, d_v=6, ctx_lo=3, ctx_hi=40, block_size=4,
+                   nb=2, q_blocks=q_blocks)
     out, lse = oracle.ragged(d["q"], d["k_nope"], d["k_rope"], d["v"], d["q_offsets"], d["kv_offsets"],
                              d["anchors"], d["block_size"])
     qo, ko = d["q_offsets"], d["kv_offsets"]
-    for r in range(5):
-        ql = qo[r + 1] - qo[r]
+    qlens = np.diff(qo)
+    if q_blocks:
+        assert len(set(qlens.tolist())) > 1 and np.any(qo[:-1] != np.arange(R) * qlens[0])
+    else:
+        assert np.all(qlens == 8)
+    for r in range(R):
         sl = slice(ko[r], ko[r + 1])
         an = d["anchors"][qo[r] // 4:qo[r + 1] // 4][None]
         o, l = oracle.anchored(d["q"][None, qo[r]:qo[r + 1]], d["k_nope"][None, sl], d["k_rope"][None, sl],
                                d["v"][None, sl], an, 4)
         np.testing.assert_allclose(out[qo[r]:qo[r + 1]], o[0], atol=TOL, rtol=0)
         np.testing.assert_allclose(lse[:, qo[r]:qo[r + 1]], l[0], atol=TOL, rtol=0)
-        assert ql == 8
+
+
+def test_ragged_mixed_lengths_against_brute_force():
+    """Mixed draft lengths against the numpy brute force, one request at a time:
+    its own keys and a mask built by hand from its anchors (context p < a_j, own
+    block only)."""
+    d = synth.make("decode_bf16", seed=7, R=6, H=2, d_nope=8, d_rope=4, d_v=6, ctx_lo=2, ctx_hi=30,
+                   block_size=3, nb=1, q_blocks=(1, 2, 4), dtype="fp32")
+    out, lse = oracle.ragged(d["q"], d["k_nope"], d["k_rope"], d["v"], d["q_offsets"], d["kv_offsets"],
+                             d["anchors"], 3)
+    qo, ko = d["q_offsets"], d["kv_offsets"]
+    for r in range(6):
+        ql, kl = int(qo[r + 1] - qo[r]), int(ko[r + 1] - ko[r])
+        S_r = kl - ql
+        mask = np.full((1, 1, ql, kl), -np.inf)
+        for i in range(ql):
+            j = i // 3
+            a = int(d["anchors"][qo[r] // 3 + j])
+            mask[0, 0, i, :a] = 0.0
+            mask[0, 0, i, S_r + 3 * j:S_r + 3 * j + 3] = 0.0
+        sl = slice(ko[r], ko[r + 1])
+        o, l = brute.dense(d["q"][None, qo[r]:qo[r + 1]], d["k_nope"][None, sl], d["k_rope"][None, sl],
+                           d["v"][None, sl], mask, oracle.default_scale(8, 4))
+        np.testing.assert_allclose(out[qo[r]:qo[r + 1]], o[0], atol=TOL, rtol=0)
+        np.testing.assert_allclose(lse[:, qo[r]:qo[r + 1]], l[0], atol=TOL, rtol=0)
 
 
 @pytest.mark.parametrize("split", [1, 7, 16, 1000])

@@ -74,17 +74,13 @@ def _small_case(dtype, B, H, S, nb, bs, dn, dr, dv, seed=123):
                       d_rope=dr, d_v=dv, anchor_lo=0, anchor_hi=S + 1)
 
 
-@pytest.fixture(params=["default", "simt", "tc1", "tc2"])
+@pytest.fixture(params=["default", "simt"])
 def kernel(request, monkeypatch):
     """Run a case on the default dispatch (tensor cores for the Kimi K3 MLA bf16
-    shape), with the exact CUDA-core kernel forced, and with each of the two
-    tensor-core kernels (one CTA per item; CTA pairs) forced."""
+    shape) and with the exact CUDA-core kernel forced."""
     monkeypatch.delenv("DFLASH_FORCE_SIMT", raising=False)
-    monkeypatch.delenv("DFLASH_TC_KERNEL", raising=False)
     if request.param == "simt":
         monkeypatch.setenv("DFLASH_FORCE_SIMT", "1")
-    elif request.param in ("tc1", "tc2"):
-        monkeypatch.setenv("DFLASH_TC_KERNEL", request.param[-1])
     return request.param
 
 
@@ -151,11 +147,9 @@ def test_dense_general_mask_with_finite_values_and_empty_rows(dfl):
     assert np.all(got_o[1, 7] == 0) and np.all(np.isneginf(got_l[1, :, 7]))
 
 
-@pytest.mark.parametrize("tc", ["1", "2"])
-def test_output_only_16_byte_aligned(dfl, tc, monkeypatch):
-    """The tensor-core kernels write rows with 32-byte stores when `out` is 32-byte
+def test_output_only_16_byte_aligned(dfl):
+    """The tensor-core kernel writes rows with 32-byte stores when `out` is 32-byte
     aligned and with 16-byte stores otherwise; both give the same bytes."""
-    monkeypatch.setenv("DFLASH_TC_KERNEL", tc)
     d = _small_case("bf16", 1, 2, 1024, 40, 16, 128, 64, 128)
     t = _dev(d, "bf16")
     an = torch.from_numpy(d["anchors"]).cuda()
@@ -306,6 +300,71 @@ def test_ragged_decode_split_context_every_row(dfl, bs, nb, seed):
     assert max_abs_err(got_l, want_l) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("dtype,dn,dr,dv,bs,q_blocks", [
+    ("bf16", 128, 64, 128, 16, (1, 2, 3)),     # max_q_len 48: one query tile per request
+    ("bf16", 128, 64, 128, 8, (1, 20, 40)),    # up to 320 rows: several query tiles, ragged tails
+    ("fp32", 16, 8, 16, 8, (1, 3, 7)),
+])
+def test_ragged_mixed_lengths_every_row(dfl, dtype, dn, dr, dv, bs, q_blocks, kernel):
+    """Requests with different draft lengths (q_offsets[r] != r * q_len), so a
+    request's anchors start at its own global block q_offsets[r] / bs."""
+    d = synth.make("decode_bf16", seed=90 + bs, dtype=dtype, R=9, H=3, d_nope=dn, d_rope=dr, d_v=dv, ctx_lo=1,
+                   ctx_hi=900, block_size=bs, q_blocks=q_blocks)
+    assert len(set(np.diff(d["q_offsets"]).tolist())) > 1
+    want_o, want_l = oracle.ragged(d["q"], d["k_nope"], d["k_rope"], d["v"], d["q_offsets"], d["kv_offsets"],
+                                   d["anchors"], bs)
+    got_o, got_l = _run_ragged(dfl, d, dtype)
+    assert not np.isnan(got_o).any() and not np.isnan(got_l).any()
+    assert max_abs_err(got_o, want_o) <= TOL[dtype]
+    assert max_abs_err(got_l, want_l) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("seed", [95, 96])
+def test_ragged_decode_mixed_lengths_split_context_every_row(dfl, seed):
+    """The split-context decode path (max_q_len <= 16) with requests of 8 and 16
+    rows and contexts that cross the 2048-key split boundaries."""
+    d = synth.make("decode_bf16", seed=seed, R=8, H=2, ctx_lo=1500, ctx_hi=9000, block_size=8, q_blocks=(1, 2))
+    assert set(np.diff(d["q_offsets"]).tolist()) == {8, 16}
+    want_o, want_l = oracle.ragged(d["q"], d["k_nope"], d["k_rope"], d["v"], d["q_offsets"], d["kv_offsets"],
+                                   d["anchors"], 8)
+    got_o, got_l = _run_ragged(dfl, d, "bf16", max_q_len=16)
+    assert not np.isnan(got_o).any() and not np.isnan(got_l).any()
+    assert max_abs_err(got_o, want_o) <= TOL["bf16"]
+    assert max_abs_err(got_l, want_l) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("path", ["decode", "tc", "simt"])
+def test_ragged_q_len_beyond_max_q_len_reported(dfl, path, monkeypatch):
+    """A request longer than the declared max_q_len is recorded as
+    DFLASH_ERR_INVALID and skipped (its rows stay unwritten) on every path; the
+    other requests are still computed."""
+    monkeypatch.delenv("DFLASH_FORCE_SIMT", raising=False)
+    if path == "simt":
+        monkeypatch.setenv("DFLASH_FORCE_SIMT", "1")
+    bs, declared = (8, 16) if path == "decode" else (16, 32)
+    nbr = np.array([1, 3, 1])  # request 1 has more rows than declared
+    ctx = np.array([300, 1200, 700])
+    qlens = nbr * bs
+    qo = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    ko = np.concatenate([[0], np.cumsum(ctx + qlens)]).astype(np.int32)
+    rng = np.random.default_rng(5)
+    an = np.concatenate([np.sort(rng.integers(0, ctx[r] + 1, size=nbr[r])) for r in range(3)]).astype(np.int32)
+    d2 = dict(q=synth._normal(97, 0, (int(qo[-1]), 2, 192), "bf16"),
+              k_nope=synth._normal(97, 1, (int(ko[-1]), 2, 128), "bf16"),
+              k_rope=synth._normal(97, 2, (int(ko[-1]), 64), "bf16"),
+              v=synth._normal(97, 3, (int(ko[-1]), 2, 128), "bf16"), total_q=int(qo[-1]))
+    t = _dev(d2, "bf16")
+    out = torch.full((d2["total_q"], 2, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    qo_t, ko_t, an_t = (torch.from_numpy(x).cuda() for x in (qo, ko, an))
+    dfl.dflash_attn_ragged(t["q"], t["k_nope"], t["k_rope"], t["v"], qo_t, ko_t, an_t, bs, declared, out=out)
+    assert dfl.dflash_last_device_error() == 1  # DFLASH_ERR_INVALID
+    got = to_numpy_f64(out)
+    assert np.isnan(got[qo[1]:qo[2]]).all()  # the long request is skipped
+    want_o, _ = oracle.ragged(d2["q"], d2["k_nope"], d2["k_rope"], d2["v"], qo, ko, an, bs)
+    for r in (0, 2):
+        assert max_abs_err(got[qo[r]:qo[r + 1]], want_o[qo[r]:qo[r + 1]]) <= TOL["bf16"]
+
+
 def test_ragged_split_equals_unsplit(dfl, monkeypatch):
     d = synth.make("decode_bf16", seed=84, R=5, H=2, ctx_lo=100, ctx_hi=6000)
     split_o, split_l = _run_ragged(dfl, d, "bf16")
@@ -362,12 +421,8 @@ def _lse_rows_batched(got_l, d, rows):
     return got_l[b, :, i]
 
 
-@pytest.mark.parametrize("name,tc", [("prefill_bf16", None), ("training_bf16", None), ("long_bf16", None),
-                                     ("prefill_bf16", "2"), ("long_bf16", "2")])
-def test_full_workload_anchored_sampled(dfl, name, tc, monkeypatch):
-    # default dispatch on every workload, then the CTA-pair kernel on the shortest and the longest
-    if tc:
-        monkeypatch.setenv("DFLASH_TC_KERNEL", tc)
+@pytest.mark.parametrize("name", ["prefill_bf16", "training_bf16", "long_bf16"])
+def test_full_workload_anchored_sampled(dfl, name):
     d = synth.make(name)
     got_o, got_l = _run_batched(dfl, d, "anchored", "bf16")
     assert not np.isnan(got_o).any()

@@ -115,6 +115,21 @@ def test_decode_recipe():
     assert abs(np.log(ctx).mean() - mid) < 0.5
 
 
+def test_mixed_draft_length_recipe():
+    d = synth.make("decode_bf16", R=40, H=1, d_nope=1, d_rope=1, d_v=1, block_size=8, q_blocks=(1, 2, 3))
+    qo, ko = d["q_offsets"].astype(np.int64), d["kv_offsets"].astype(np.int64)
+    ctx = d["context_lens"].astype(np.int64)
+    qlens = np.diff(qo)
+    assert set(qlens.tolist()) == {8, 16, 24}  # every count drawn at least once among 40 requests
+    assert qo[0] == 0 and np.all(qo % 8 == 0) and d["total_q"] == qo[-1]
+    np.testing.assert_array_equal(np.diff(ko), ctx + qlens)
+    assert d["anchors"].size == qo[-1] // 8
+    for r in range(40):
+        a = d["anchors"][qo[r] // 8:qo[r + 1] // 8]
+        assert np.all(np.diff(a) >= 0) and a.min() >= 0 and a[-1] == ctx[r]
+    assert d["q"].shape == (qo[-1], 1, 2) and d["k_nope"].shape == (ko[-1], 1, 1)
+
+
 def test_dout_is_its_own_stream():
     d = synth.make("tiny_fp32")
     g1, g2 = synth.make_dout(d), synth.make_dout(d)

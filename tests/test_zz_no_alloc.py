@@ -55,8 +55,13 @@ def test_noalloc_dense_matches_workspace_dense_on_two_calls(dfl):
         lse = torch.full((B, H, Q), float("nan"), dtype=torch.float32, device="cuda")
         dfl.dflash_attn_dense_noalloc(t["q"], t["k_nope"], t["k_rope"], t["v"], mk, out=out, lse=lse)
         assert dfl.dflash_last_device_error() == 0
-        assert max_abs_err(to_numpy_f64(out), to_numpy_f64(ref_o)) <= TOL["bf16"]
-        assert max_abs_err(to_numpy_f64(lse), to_numpy_f64(ref_l)) <= TOL["bf16"]
+        # the same kernels on the same inputs: byte-identical results
+        assert torch.equal(out.view(torch.int16), ref_o.view(torch.int16))
+        assert torch.equal(lse, ref_l)
+        # and both within the bf16 bar of the fp64 oracle on this mask
+        want_o, want_l = oracle.dense(d["q"], d["k_nope"], d["k_rope"], d["v"], bf16_mask(m))
+        assert max_abs_err(to_numpy_f64(out), want_o) <= TOL["bf16"]
+        assert max_abs_err(to_numpy_f64(lse), want_l) <= TOL["bf16"]
 
 
 def test_noalloc_rejects_problems_beyond_its_fixed_scratch(dfl):
