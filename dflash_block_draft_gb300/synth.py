@@ -15,7 +15,12 @@ Recipe (shared by every workload):
   count; bf16 workloads round them to bf16 (nearest, ties to even).
 Anchors are sorted, distinct and uniform without replacement over the stated
 range.  bf16 tensors are carried as uint16 bit patterns.  The backward pass
-takes its output gradient dout from the same recipe as tensor id 4.
+takes its output gradient dout from the same recipe as tensor id 4.  The
+compressed-latent decode workload draws the per-token KV latent c_kv as tensor
+id 5 and the per-head expansion weight w_kv_b (kv_b_proj viewed as
+[H, d_nope + d_v, kv_rank]) as tensor id 6, standard normals scaled by
+kv_rank^-0.5 in fp32 before the bf16 rounding, so that the expanded keys and
+values have unit variance like the other workloads' inputs.
 """
 from __future__ import annotations
 
@@ -51,6 +56,10 @@ class Workload:
     # ragged only: when set, request r has nb_r blocks drawn uniformly from these
     # counts (instead of nb each), and its anchors are drawn inside its context
     q_blocks: tuple = ()
+    # ragged only: when > 0, keys and values come as compressed latents
+    # c_kv [total_kv, kv_rank] plus the per-head expansion weight
+    # w_kv_b [H, d_nope + d_v, kv_rank] instead of k_nope and v
+    kv_rank: int = 0
 
     @property
     def Q(self) -> int:
@@ -82,6 +91,9 @@ WORKLOADS = {
                  pad=_LONG_PAD),
         Workload("decode_bf16", 4, "bf16", H=32, d_nope=128, d_rope=64, d_v=128, R=64,
                  block_size=16, nb=1, ctx_lo=1024, ctx_hi=32768),
+        # the decode workload with the keys and values in compressed-latent form
+        Workload("decode_latent_bf16", 5, "bf16", H=32, d_nope=128, d_rope=64, d_v=128, R=64,
+                 block_size=16, nb=1, ctx_lo=1024, ctx_hi=32768, kv_rank=512),
     )
 }
 
@@ -106,7 +118,7 @@ def bf16_bits_to_f32(x: np.ndarray) -> np.ndarray:
 _CHUNK = 1 << 22
 
 
-def _normal(seed: int, tensor_id: int, shape, dtype: str) -> np.ndarray:
+def _normal(seed: int, tensor_id: int, shape, dtype: str, scale: float = 1.0) -> np.ndarray:
     n = int(np.prod(shape))
     out = np.empty(n, np.uint16 if dtype == "bf16" else np.float32)
 
@@ -114,6 +126,8 @@ def _normal(seed: int, tensor_id: int, shape, dtype: str) -> np.ndarray:
         lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
         g = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(tensor_id, c))))
         a = g.standard_normal(size=hi - lo, dtype=np.float32)
+        if scale != 1.0:
+            a = a * np.float32(scale)
         out[lo:hi] = f32_to_bf16_bits(a) if dtype == "bf16" else a
 
     nchunks = -(-n // _CHUNK)
@@ -178,9 +192,14 @@ def make(w: Workload | str, seed: int | None = None, **override) -> dict:
         d.update(R=w.R, q_offsets=q_off.astype(np.int32), kv_offsets=kv_off.astype(np.int32),
                  anchors=anchors, context_lens=ctx.astype(np.int32), total_q=total_q, total_kv=total_kv,
                  q=_normal(seed, 0, (total_q, w.H, dqk), w.dtype),
-                 k_nope=_normal(seed, 1, (total_kv, w.H, w.d_nope), w.dtype),
-                 k_rope=_normal(seed, 2, (total_kv, w.d_rope), w.dtype),
-                 v=_normal(seed, 3, (total_kv, w.H, w.d_v), w.dtype))
+                 k_rope=_normal(seed, 2, (total_kv, w.d_rope), w.dtype))
+        if w.kv_rank:
+            d.update(kv_rank=w.kv_rank, c_kv=_normal(seed, 5, (total_kv, w.kv_rank), w.dtype),
+                     w_kv_b=_normal(seed, 6, (w.H, w.d_nope + w.d_v, w.kv_rank), w.dtype,
+                                    scale=w.kv_rank ** -0.5))
+        else:
+            d.update(k_nope=_normal(seed, 1, (total_kv, w.H, w.d_nope), w.dtype),
+                     v=_normal(seed, 3, (total_kv, w.H, w.d_v), w.dtype))
         return d
     K = w.S + w.Q
     anchors = np.stack([sorted_distinct(rng, w.anchor_lo, w.anchor_hi, w.nb) for _ in range(w.B)])

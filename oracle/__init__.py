@@ -57,11 +57,12 @@ def _load():
             lib.oracle_build_mask.argtypes = [I, I, I, P, I, I, P]
             lib.oracle_tile_classes.argtypes = [I, I, I, I, I, P, I, I, P, I, P]
             lib.oracle_max_threads.argtypes = []
+            lib.oracle_latent_expand.argtypes = [I, I, I, I, I, P, P, I64, I64, P, P, I]
             lib.oracle_backward.argtypes = [I, I, I, I, I, I, I, D, I, P, P, P, P, P, P, I, I, P, I, P, I64,
                                             P, P, P, P, I]
             for f in (lib.oracle_dense, lib.oracle_anchored, lib.oracle_ragged,
                       lib.oracle_anchored_split, lib.oracle_build_mask, lib.oracle_tile_classes,
-                      lib.oracle_max_threads, lib.oracle_backward):
+                      lib.oracle_max_threads, lib.oracle_backward, lib.oracle_latent_expand):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -275,3 +276,64 @@ def tile_classes(B, S, Q, tile_m, tile_n, anchors=None, block_size=0, mask=None)
     if rc:
         raise ValueError("oracle_tile_classes failed")
     return out
+
+
+def latent_expand(c_kv, w_kv_b, d_nope, t0=0, t1=None, nthreads=0):
+    """Expand compressed KV latents to per-head keys and values (fp64).
+
+    c_kv [T, rank], w_kv_b [H, d_nope + d_v, rank] (the kv_b_proj weight per
+    head: key rows first, then value rows).  Returns k_nope [t1-t0, H, d_nope]
+    and v [t1-t0, H, d_v] for tokens [t0, t1)."""
+    c_kv, w_kv_b = _c(c_kv), _c(w_kv_b)
+    T, rank = c_kv.shape
+    H, E, rank2 = w_kv_b.shape
+    assert rank2 == rank and 0 <= d_nope < E
+    dt = _same_dtype(c_kv, w_kv_b)
+    t1 = T if t1 is None else int(t1)
+    kn = np.empty((t1 - t0, H, d_nope), np.float64)
+    v = np.empty((t1 - t0, H, E - d_nope), np.float64)
+    rc = _load().oracle_latent_expand(H, d_nope, E - d_nope, rank, dt, _ptr(c_kv), _ptr(w_kv_b), int(t0), t1,
+                                      _ptr(kn), _ptr(v), nthreads)
+    if rc:
+        raise ValueError("oracle_latent_expand failed")
+    return kn, v
+
+
+def _to_f64(a):
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def latent_ragged(q, c_kv, k_rope, w_kv_b, q_offsets, kv_offsets, anchors, block_size, scale=None,
+                  requests=None, nthreads=0):
+    """Ragged anchored attention whose per-head keys and values are the
+    expansions of compressed KV latents (see oracle_latent_expand): expand,
+    then evaluate the ragged definition, all in fp64.
+
+    q [total_q, H, d_nope+d_rope], c_kv [total_kv, rank], k_rope [total_kv, d_rope],
+    w_kv_b [H, d_nope+d_v, rank].  scale defaults to (d_nope+d_rope)^-0.5.
+    requests: optional subset of request indices (their rows only; others 0).
+    Returns out [total_q, H, d_v] and lse [H, total_q] (rows of requests not
+    evaluated are 0 and -inf)."""
+    qo, ko, an = _c(q_offsets, np.int32), _c(kv_offsets, np.int32), _c(anchors, np.int32)
+    R = qo.size - 1
+    TQ, H, dqk = np.asarray(q).shape
+    d_rope = np.asarray(k_rope).shape[1]
+    d_nope = dqk - d_rope
+    dv = np.asarray(w_kv_b).shape[1] - d_nope
+    scale = default_scale(d_nope, d_rope) if scale is None else float(scale)
+    out = np.zeros((TQ, H, dv), np.float64)
+    lse = np.full((H, TQ), -np.inf)
+    for r in (range(R) if requests is None else requests):
+        k0, k1, q0, q1 = int(ko[r]), int(ko[r + 1]), int(qo[r]), int(qo[r + 1])
+        kn, v = latent_expand(c_kv, w_kv_b, d_nope, k0, k1, nthreads=nthreads)
+        kr = _to_f64(np.asarray(k_rope)[k0:k1])
+        qq = _to_f64(np.asarray(q)[q0:q1])
+        an_r = an[q0 // block_size:q1 // block_size]
+        o, l = ragged(qq, kn, kr, v, np.array([0, q1 - q0], np.int32), np.array([0, k1 - k0], np.int32), an_r,
+                      block_size, scale=scale, nthreads=nthreads)
+        out[q0:q1] = o
+        lse[:, q0:q1] = l
+    return out, lse

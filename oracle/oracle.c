@@ -550,5 +550,40 @@ int oracle_tile_classes(int B, int S, int Q, int tile_m, int tile_n, const int32
   return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Compressed-latent MLA: the per-head keys and values a token's latent        */
+/* expands to.  The attention's kv_b_proj maps each token's KV latent c        */
+/* (kv_lora_rank values, after kv_a_layernorm) to one qk_nope + v slice per     */
+/* head (KimiK3DSparkAttention attributes on the DSpark Kimi K3 draft page;    */
+/* KimiK3DFlashAttention on the DFlash Kimi K3 draft page: kv_b_proj produces  */
+/* num_attention_heads slices of qk_nope_head_dim + v_head_dim).  With that    */
+/* projection's weight viewed per head as w[h, e, c] (e < dn: the key part,     */
+/* e >= dn: the value part; c < rank):                                         */
+/*   k_nope[t,h,e] = sum_c w[h, e, c]      c_kv[t, c]    (e < dn)              */
+/*   v[t,h,e]      = sum_c w[h, dn + e, c] c_kv[t, c]    (e < dv)              */
+/* The rope part of the key stays the head-shared k_rope[t] (the latent holds  */
+/* kv_lora_rank + qk_rope_head_dim values per token: Kimi K3 target page, MLA  */
+/* context-parallel attention).  Attention over the expanded keys and values  */
+/* is then the ragged definition above.  Tokens [t0, t1) are expanded into     */
+/* fp64 k_nope_out [t1-t0, H, dn] and v_out [t1-t0, H, dv].                    */
+/* ------------------------------------------------------------------------ */
+int oracle_latent_expand(int H, int dn, int dv, int rank, int dt, const void* c_kv, const void* w,
+                         int64_t t0, int64_t t1, double* k_nope_out, double* v_out, int nthreads) {
+  if (H <= 0 || dn < 0 || dv <= 0 || rank <= 0 || t1 < t0) return 1;
+  const int E = dn + dv;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads_or_default(nthreads))
+  for (int64_t t = t0; t < t1; ++t) {
+    for (int h = 0; h < H; ++h)
+      for (int e = 0; e < E; ++e) {
+        double acc = 0.0;
+        for (int c = 0; c < rank; ++c)
+          acc += ld(w, dt, ((size_t)h * E + e) * (size_t)rank + c) * ld(c_kv, dt, (size_t)t * rank + c);
+        if (e < dn) k_nope_out[((size_t)(t - t0) * H + h) * dn + e] = acc;
+        else v_out[((size_t)(t - t0) * H + h) * dv + (e - dn)] = acc;
+      }
+  }
+  return 0;
+}
+
 /* Number of OpenMP threads a parallel region gets by default. */
 int oracle_max_threads(void) { return nthreads_or_default(0); }
