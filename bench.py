@@ -14,8 +14,9 @@ The same JSON line carries a ``per_config`` block: every other workload of the
 suite measured the same way on the same GPU -- bf16 prefill and training
 (anchored and dense-mask entry points), long context through the dense mask,
 the ragged serving decode (algorithmic HBM GB/s against the measured HBM
-peak) and the tiny fp32 case (its parity against the fp64 oracle, computed in
-the CPU-baseline leg).
+peak), the same decode with keys and values as compressed MLA latents
+(absorbed-form TFLOP/s) and the tiny fp32 case (its parity against the fp64
+oracle, computed in the CPU-baseline leg).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload W] [--mode anchored|dense] [--pass forward|backward]
@@ -56,7 +57,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # The rest of the suite, reported beside the headline: (workload, entry point).
 PER_CONFIG = (("prefill_bf16", "anchored"), ("prefill_bf16", "dense"), ("training_bf16", "anchored"),
               ("training_bf16", "dense"), ("long_bf16", "dense"), ("decode_bf16", "ragged"),
-              ("tiny_fp32", "anchored"))
+              ("decode_latent_bf16", "latent"), ("tiny_fp32", "anchored"))
 # Targets: prefill-shaped workloads at >= 50 % of the bf16 tensor peak, the
 # ragged decode at >= 60 % of HBM bandwidth.
 TARGET_FRAC = {"tensor": 0.50, "hbm": 0.60}
@@ -575,6 +576,45 @@ def measure_decode(dfl, steps, warmup, device, world, peaks, requests=None):
             "gpu_launches": launches, "clocks": clocks}
 
 
+def measure_latent(dfl, steps, warmup, device, world, peaks, requests=None):
+    """The decode workload with keys and values as compressed latents (kv_lora_rank
+    512): query absorption, latent attention, split merge and output projection.
+    Bound by the tensor cores: the roofline is the absorbed form's FLOPs."""
+    import torch
+    d = synth.make("decode_latent_bf16", **({"R": requests} if requests else {}))
+    H, bs, rank = d["H"], d["block_size"], d["kv_rank"]
+    work = metrics.latent_work(d["q_offsets"], d["kv_offsets"], d["anchors"], H, bs, d["d_nope"], d["d_rope"],
+                               d["d_v"], rank)
+    dev = {k: to_dev(d[k], "bf16", device) for k in ("q", "c_kv", "k_rope", "w_kv_b")}
+    qo, ko, an = (torch.from_numpy(d[k]).to(device) for k in ("q_offsets", "kv_offsets", "anchors"))
+    out = torch.empty((d["total_q"], H, d["d_v"]), dtype=torch.bfloat16, device=device)
+    nbytes = dfl.dflash_attn_latent_workspace_size(d["R"], H, d["d_nope"], d["d_rope"], d["d_v"], rank,
+                                                   dfl.DFLASH_BF16, d["total_q"], d["total_kv"], 16)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def step():
+        dfl.dflash_attn_latent_ragged(dev["q"], dev["c_kv"], dev["k_rope"], dev["w_kv_b"], qo, ko, an, bs, 16,
+                                      out=out, workspace=ws, stream=stream)
+
+    times, launches, clocks = timed_loop(step, steps, warmup, device, stream, flush, world, dfl)
+    kernel_ms = sum(times) / len(times)
+    ms = max_over_ranks(kernel_ms, world, device)
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = work["flops"] / (kernel_ms / 1e3) / 1e12
+    return {"workload": workload_desc(d) + f", kv_rank={rank} (compressed latents)",
+            "value": job_value(work["flops"], world, ms) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "steps": steps, "gbs": work["bytes"] / (kernel_ms / 1e3) / 1e9,
+            "unmasked_flops_per_step": work["flops"], "algorithmic_bytes_per_step": work["bytes"],
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak,
+                         "kernel": "q absorption GEMM + split plan + latent attention + merge + output projection GEMM",
+                         "flops_note": "2*(kv_rank+d_rope) + 2*kv_rank per visible (row, key, head), plus "
+                                       "2*kv_rank*(d_nope+d_v) per (row, head)"},
+            "gpu_launches": launches, "clocks": clocks}
+
+
 def release_memory():
     import gc
 
@@ -602,6 +642,11 @@ def run_ours(args):
         metric = "DFlash block-attn ragged decode: algorithmic HBM GB/s (and unmasked TFLOP/s)"
         d_head = None
         head["roofline"]["peak_source"] = f"hbm_gbs ({peak_src})"
+    elif args.workload == "decode_latent_bf16":
+        head = measure_latent(dfl, args.steps, args.warmup, device, world, peaks, args.requests)
+        metric = "DFlash block-attn compressed-latent decode: TFLOP/s (absorbed-form FLOPs)"
+        d_head = None
+        head["roofline"]["peak_source"] = f"bf16_tflops ({peak_src})"
     else:
         d_head = synth.make(args.workload, **({"H": args.heads} if args.heads else {}))
         head = measure_batched(dfl, d_head, args.mode, backward, args.steps, args.warmup, device, world, peaks,
@@ -622,6 +667,8 @@ def run_ours(args):
         for w, mode in PER_CONFIG:
             if w == "decode_bf16":
                 r = measure_decode(dfl, args.steps, args.warmup, device, 1, peaks)
+            elif w == "decode_latent_bf16":
+                r = measure_latent(dfl, args.steps, args.warmup, device, 1, peaks)
             else:
                 dw = synth.make(w)
                 r = measure_batched(dfl, dw, mode, False, args.steps, args.warmup, device, 1, peaks,
@@ -703,7 +750,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="measure the headline workload only (no per_config block)")
-    ap.add_argument("--workload", choices=["long_bf16", "prefill_bf16", "training_bf16", "decode_bf16", "tiny_fp32"],
+    ap.add_argument("--workload", choices=["long_bf16", "prefill_bf16", "training_bf16", "decode_bf16",
+                                           "decode_latent_bf16", "tiny_fp32"],
                     default=WORKLOAD,
                     help="long_bf16 (the largest workload) is the headline; the others are the rest of the suite "
                          "(decode_bf16 is HBM-bound and reported in GB/s)")
@@ -716,7 +764,7 @@ def main(argv=None):
                     help="batched workloads only: use this many heads instead of the workload's (same recipe "
                          "otherwise; for profiling captures that must stay small)")
     ap.add_argument("--requests", type=int, default=None,
-                    help="decode_bf16 only: draw this many requests instead of 64 (same recipe; "
+                    help="decode workloads only: draw this many requests instead of 64 (same recipe; "
                          "for profiling captures that must stay small)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

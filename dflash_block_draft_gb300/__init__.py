@@ -36,7 +36,8 @@ STATUS = {0: "DFLASH_OK", 1: "DFLASH_ERR_INVALID", 2: "DFLASH_ERR_SHAPE", 3: "DF
 EXPORTS = ("dflash_attn_dense", "dflash_attn_anchored", "dflash_attn_ragged", "dflash_attn_workspace_size",
            "dflash_build_schedule_host", "dflash_scan_mask", "dflash_status_string", "dflash_last_device_error",
            "dflash_kernel_launches", "dflash_attn_dense_noalloc", "dflash_build_mask",
-           "dflash_attn_anchored_backward", "dflash_attn_dense_backward", "dflash_test_inject_stall")
+           "dflash_attn_anchored_backward", "dflash_attn_dense_backward", "dflash_test_inject_stall",
+           "dflash_attn_latent_ragged", "dflash_attn_latent_workspace_size")
 
 
 class DFlashError(RuntimeError):
@@ -86,6 +87,11 @@ def load_library(path: str | None = None):
         lib.dflash_attn_dense_backward.argtypes = [DP, I, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P]
         lib.dflash_attn_anchored_backward.restype = ctypes.c_int
         lib.dflash_attn_dense_backward.restype = ctypes.c_int
+        lib.dflash_attn_latent_ragged.argtypes = [I, I, I, I, I, I, F, I, P, P, P, P, P, P, P, I, I, I, I, P, P, P,
+                                                  S, P]
+        lib.dflash_attn_latent_ragged.restype = ctypes.c_int
+        lib.dflash_attn_latent_workspace_size.argtypes = [I, I, I, I, I, I, I, I, I, I]
+        lib.dflash_attn_latent_workspace_size.restype = S
         lib.dflash_test_inject_stall.argtypes = [ctypes.c_ulonglong, I]
         lib.dflash_test_inject_stall.restype = None
         lib.dflash_kernel_launches.argtypes = []
@@ -276,6 +282,46 @@ def dflash_attn_ragged(q, k_nope, k_rope, v, q_offsets, kv_offsets, anchors, blo
                                 int(max_q_len), _dev_ptr(out, "out", q.dtype), _dev_ptr(lse, "lse", torch.float32),
                                 _dev_ptr(ws, "workspace"), nbytes, _stream(stream))
     _check("dflash_attn_ragged", st)
+    return out
+
+
+def dflash_attn_latent_workspace_size(R, H, d_nope, d_rope, d_v, kv_rank, dtype=DFLASH_BF16, total_q=0,
+                                      total_kv=0, max_q_len=0) -> int:
+    return int(load_library().dflash_attn_latent_workspace_size(R, H, d_nope, d_rope, d_v, kv_rank, dtype, total_q,
+                                                                 total_kv, max_q_len))
+
+
+def dflash_attn_latent_ragged(q, c_kv, k_rope, w_kv_b, q_offsets, kv_offsets, anchors, block_size, max_q_len,
+                              out=None, lse=None, scale=0.0, workspace=None, stream=None):
+    """Ragged block attention over compressed KV latents.  q [total_q,H,dn+dr],
+    c_kv [total_kv,kv_rank], k_rope [total_kv,dr], w_kv_b [H,dn+dv,kv_rank]
+    (kv_b_proj per head: key rows, then value rows); offsets int32 [R+1] and
+    anchors int32 [total_q/block_size] on the device.  lse is [H,total_q]."""
+    torch = _torch()
+    lib = load_library()
+    total_q, H, dqk = q.shape
+    total_kv, rank = c_kv.shape
+    dr = k_rope.shape[1]
+    dn = dqk - dr
+    if w_kv_b.shape[0] != H or w_kv_b.shape[2] != rank or w_kv_b.shape[1] <= dn or k_rope.shape[0] != total_kv:
+        raise ValueError("inconsistent q / c_kv / k_rope / w_kv_b shapes")
+    dv = w_kv_b.shape[1] - dn
+    R = q_offsets.shape[0] - 1
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty((total_q, H, dv), dtype=q.dtype, device=q.device)
+    nbytes = dflash_attn_latent_workspace_size(R, H, dn, dr, dv, rank, dt, total_q, total_kv, int(max_q_len))
+    ws = _workspace(nbytes, workspace, q.device)
+    st = lib.dflash_attn_latent_ragged(R, H, dn, dr, dv, rank, float(scale or 0.0), dt, _dev_ptr(q, "q"),
+                                       _dev_ptr(c_kv, "c_kv", q.dtype), _dev_ptr(k_rope, "k_rope", q.dtype),
+                                       _dev_ptr(w_kv_b, "w_kv_b", q.dtype),
+                                       _dev_ptr(q_offsets, "q_offsets", torch.int32),
+                                       _dev_ptr(kv_offsets, "kv_offsets", torch.int32),
+                                       _dev_ptr(anchors, "anchors", torch.int32), int(block_size), total_q, total_kv,
+                                       int(max_q_len), _dev_ptr(out, "out", q.dtype),
+                                       _dev_ptr(lse, "lse", torch.float32), _dev_ptr(ws, "workspace"), nbytes,
+                                       _stream(stream))
+    _check("dflash_attn_latent_ragged", st)
     return out
 
 

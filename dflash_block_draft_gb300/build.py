@@ -21,7 +21,7 @@ LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libdflash_attn.so")
 
 SOURCES = ["api.cu", "attn_simt.cu", "attn_tc.cu", "mask_scan.cu", "dense_noalloc.cu",
-           "attn_decode.cu", "attn_bwd.cu", "attn_bwd_tc.cu"]
+           "attn_decode.cu", "attn_bwd.cu", "attn_bwd_tc.cu", "attn_latent.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -191,6 +191,77 @@ cudaError_t launch_tc(const AttnParams& p, int segments, int nqt, long long q_ro
   return launch_attn_tc(p, segments, nqt, q_rows, kv_rows, stream);
 }
 
+dflash_status_t check_ragged(int R, int H, int d_nope, int d_rope, int d_v, float scale, dflash_dtype_t dtype,
+                             int block_size, int total_q, int total_kv, int max_q_len) {
+  dflash_status_t st;
+  if ((st = check_dtype(dtype)) != DFLASH_OK) return st;
+  if (R < 0 || total_q < 0 || total_kv < 0 || max_q_len < 0 || block_size <= 0) return DFLASH_ERR_SHAPE;
+  if ((st = check_heads(H, d_nope, d_rope, d_v)) != DFLASH_OK) return st;
+  if (isnan(scale) || isinf(scale)) return DFLASH_ERR_INVALID;
+  if (R > 65535 || H > 65535) return DFLASH_ERR_UNSUPPORTED;
+  return DFLASH_OK;
+}
+
+AttnParams ragged_params(int R, int H, int dn, int dr, int dv, float scale, const void* q, const void* kn,
+                         const void* kr, const void* v, const int32_t* q_offsets, const int32_t* kv_offsets,
+                         const int32_t* anchors, int bs, int total_q, int total_kv, int max_q_len, void* out,
+                         float* lse) {
+  AttnParams p = base_params(H, dn, dr, dv, scale, q, kn, kr, v, out, lse);
+  p.mode = kRagged;
+  p.R = R;
+  p.total_q = total_q;
+  p.total_kv = total_kv;
+  p.max_q = max_q_len;
+  p.q_off = q_offsets;
+  p.kv_off = kv_offsets;
+  p.anchors = anchors;
+  p.bs = bs;
+  return p;
+}
+
+// Kernel choice for a validated ragged call: the split-context decode kernels,
+// the tensor-core kernel, or the exact CUDA-core kernel.
+dflash_status_t ragged_dispatch(const AttnParams& p, dflash_dtype_t dtype, bool decode, void* decode_ws,
+                                cudaStream_t stream) {
+  if (decode && (long long)p.total_q + kTileM < (1ll << 31) && (long long)p.total_kv + kTileN < (1ll << 31))
+    return launched(launch_attn_decode(p, decode_ws, stream));
+  if (use_tc(dtype, p.dn, p.dr, p.dv, p.total_q, p.total_kv))
+    return launched(launch_tc(p, p.R, (p.max_q + kTileM - 1) / kTileM, p.total_q, p.total_kv, stream));
+  return launched(launch_attn_simt(p, dtype == DFLASH_BF16, p.R, p.max_q, stream));
+}
+
+// Workspace of the compressed-latent entry point: the absorbed tensor-core
+// path's buffers, or the expanded keys and values plus the ragged kernels'
+// workspace.  DFLASH_LATENT_EXPAND=1 (tests) forces the expanded path.
+struct LatentLayout {
+  bool absorbed = false, decode = false;
+  size_t absorbed_ws = 0, kn = 0, v = 0, ragged_ws = 0, total = 0;
+};
+
+LatentLayout layout_latent(int R, int H, int dn, int dr, int dv, int rank, dflash_dtype_t dtype, int total_q,
+                           int total_kv, int max_q_len) {
+  LatentLayout L;
+  L.absorbed = dtype == DFLASH_BF16 && latent_absorbed_supported(H, dn, dr, dv, rank, max_q_len) &&
+               !env_flag("DFLASH_FORCE_SIMT") && !env_flag("DFLASH_LATENT_EXPAND") &&
+               (long long)total_q + kTileM < (1ll << 31) && (long long)total_kv + kTileN < (1ll << 31);
+  size_t off = kAlign;
+  if (L.absorbed) {
+    L.absorbed_ws = off;
+    off += round_up(latent_absorbed_bytes(R, H, total_q, total_kv));
+  } else {
+    const bool bf16 = dtype == DFLASH_BF16;
+    L.kn = off;
+    off += round_up((size_t)total_kv * H * dn * (bf16 ? 2 : 4));
+    L.v = off;
+    off += round_up((size_t)total_kv * H * dv * (bf16 ? 2 : 4));
+    L.decode = use_decode(dtype, dn, dr, dv, max_q_len);
+    L.ragged_ws = off;
+    off += L.decode ? round_up(decode_workspace_bytes(R, H, total_kv)) : 0;
+  }
+  L.total = off;
+  return L;
+}
+
 }  // namespace
 }  // namespace dflash
 
@@ -350,11 +421,9 @@ dflash_status_t dflash_attn_ragged(int R, int H, int d_nope, int d_rope, int d_v
                                    int max_q_len, void* out, float* lse, void* workspace, size_t ws_bytes,
                                    dflash_stream_t stream) {
   dflash_status_t st;
-  if ((st = check_dtype(dtype)) != DFLASH_OK) return st;
-  if (R < 0 || total_q < 0 || total_kv < 0 || max_q_len < 0 || block_size <= 0) return DFLASH_ERR_SHAPE;
-  if ((st = check_heads(H, d_nope, d_rope, d_v)) != DFLASH_OK) return st;
-  if (isnan(scale) || isinf(scale)) return DFLASH_ERR_INVALID;
-  if (R > 65535 || H > 65535) return DFLASH_ERR_UNSUPPORTED;
+  if ((st = check_ragged(R, H, d_nope, d_rope, d_v, scale, dtype, block_size, total_q, total_kv, max_q_len)) !=
+      DFLASH_OK)
+    return st;
   if (R == 0 || total_q == 0) return DFLASH_OK;
   if ((st = check_tensors(q, k_nope, k_rope, v, out, lse, d_rope)) != DFLASH_OK) return st;
   if (!q_offsets || !kv_offsets || !anchors) return DFLASH_ERR_INVALID;
@@ -362,22 +431,55 @@ dflash_status_t dflash_attn_ragged(int R, int H, int d_nope, int d_rope, int d_v
   const bool decode = use_decode(dtype, d_nope, d_rope, d_v, max_q_len);
   const Layout L = layout_ragged(R, H, decode, total_kv);
   if ((st = check_workspace(workspace, ws_bytes, L.total)) != DFLASH_OK) return st;
-  AttnParams p = base_params(H, d_nope, d_rope, d_v, scale, q, k_nope, k_rope, v, out, lse);
-  p.mode = kRagged;
-  p.R = R;
-  p.total_q = total_q;
-  p.total_kv = total_kv;
-  p.max_q = max_q_len;
-  p.q_off = q_offsets;
-  p.kv_off = kv_offsets;
-  p.anchors = anchors;
-  p.bs = block_size;
-  if (decode && (long long)total_q + kTileM < (1ll << 31) && (long long)total_kv + kTileN < (1ll << 31))
-    return launched(launch_attn_decode(p, static_cast<uint8_t*>(workspace) + kAlign, (cudaStream_t)stream));
-  if (use_tc(dtype, d_nope, d_rope, d_v, total_q, total_kv))
-    return launched(launch_tc(p, R, (max_q_len + kTileM - 1) / kTileM, total_q, total_kv,
-                                   (cudaStream_t)stream));
-  return launched(launch_attn_simt(p, dtype == DFLASH_BF16, R, max_q_len, (cudaStream_t)stream));
+  AttnParams p = ragged_params(R, H, d_nope, d_rope, d_v, scale, q, k_nope, k_rope, v, q_offsets, kv_offsets, anchors,
+                               block_size, total_q, total_kv, max_q_len, out, lse);
+  return ragged_dispatch(p, dtype, decode, static_cast<uint8_t*>(workspace) + kAlign, (cudaStream_t)stream);
+}
+
+size_t dflash_attn_latent_workspace_size(int R, int H, int d_nope, int d_rope, int d_v, int kv_rank,
+                                         dflash_dtype_t dtype, int total_q, int total_kv, int max_q_len) {
+  if (check_dtype(dtype) != DFLASH_OK || R <= 0 || check_heads(H, d_nope, d_rope, d_v) != DFLASH_OK ||
+      kv_rank <= 0 || kv_rank > DFLASH_MAX_KV_RANK || total_q < 0 || total_kv < 0 || max_q_len < 0)
+    return 0;
+  return layout_latent(R, H, d_nope, d_rope, d_v, kv_rank, dtype, total_q, total_kv, max_q_len).total;
+}
+
+dflash_status_t dflash_attn_latent_ragged(int R, int H, int d_nope, int d_rope, int d_v, int kv_rank, float scale,
+                                          dflash_dtype_t dtype, const void* q, const void* c_kv, const void* k_rope,
+                                          const void* w_kv_b, const int32_t* q_offsets, const int32_t* kv_offsets,
+                                          const int32_t* anchors, int block_size, int total_q, int total_kv,
+                                          int max_q_len, void* out, float* lse, void* workspace, size_t ws_bytes,
+                                          dflash_stream_t stream) {
+  dflash_status_t st;
+  if ((st = check_ragged(R, H, d_nope, d_rope, d_v, scale, dtype, block_size, total_q, total_kv, max_q_len)) !=
+      DFLASH_OK)
+    return st;
+  if (kv_rank <= 0) return DFLASH_ERR_SHAPE;
+  if (kv_rank > DFLASH_MAX_KV_RANK) return DFLASH_ERR_UNSUPPORTED;
+  if (R == 0 || total_q == 0) return DFLASH_OK;
+  if (!q || !c_kv || !w_kv_b || !out || (d_rope > 0 && !k_rope)) return DFLASH_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(c_kv) || !aligned16(w_kv_b) || !aligned16(out) || (d_rope > 0 && !aligned16(k_rope)))
+    return DFLASH_ERR_ALIGN;
+  if (lse && ((uintptr_t)lse & 3u)) return DFLASH_ERR_ALIGN;
+  if (!q_offsets || !kv_offsets || !anchors) return DFLASH_ERR_INVALID;
+  if (max_q_len == 0) return DFLASH_ERR_SHAPE;
+  const LatentLayout L = layout_latent(R, H, d_nope, d_rope, d_v, kv_rank, dtype, total_q, total_kv, max_q_len);
+  if ((st = check_workspace(workspace, ws_bytes, L.total)) != DFLASH_OK) return st;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (L.absorbed) {
+    AttnParams p = ragged_params(R, H, d_nope, d_rope, d_v, scale, q, nullptr, k_rope, nullptr, q_offsets,
+                                 kv_offsets, anchors, block_size, total_q, total_kv, max_q_len, out, lse);
+    return launched(launch_latent_absorbed(p, c_kv, w_kv_b, w + L.absorbed_ws, s));
+  }
+  // Expanded: per-head keys and values in the workspace, then the ragged kernels.
+  void* kn = w + L.kn;
+  void* vv = w + L.v;
+  cudaError_t e = launch_latent_expand(c_kv, w_kv_b, dtype == DFLASH_BF16, total_kv, H, d_nope, d_v, kv_rank, kn, vv, s);
+  if (e != cudaSuccess) return DFLASH_ERR_CUDA;
+  AttnParams p = ragged_params(R, H, d_nope, d_rope, d_v, scale, q, kn, k_rope, vv, q_offsets, kv_offsets, anchors,
+                               block_size, total_q, total_kv, max_q_len, out, lse);
+  return ragged_dispatch(p, dtype, L.decode, w + L.ragged_ws, s);
 }
 
 }  // extern "C"

@@ -53,6 +53,10 @@ cudaError_t launch_attn_simt(const AttnParams& p, bool bf16, int segments, int m
 // TMA tensor maps over bf16 tensors, 128-byte swizzle, box {64, 1, box_rows} / {64, box_rows}.
 bool make_map_3d(CUtensorMap* m, const void* base, long long rows, int heads, int width, int box_rows);
 bool make_map_2d(CUtensorMap* m, const void* base, long long rows, int width, int box_rows);
+// General 3-D bf16 map, 128-byte swizzle: dims innermost first, byte strides of
+// dims 1 and 2, box extents (box[0] * 2 bytes = 128).
+bool make_map_3d_box(CUtensorMap* m, const void* base, const unsigned long long dims[3],
+                     const unsigned long long strides_bytes[2], const unsigned box[3]);
 int sm_count();
 
 bool tc_supported(int dn, int dr, int dv);
@@ -81,6 +85,19 @@ bool bwd_tc_supported(int dn, int dr, int dv);
 cudaError_t launch_attn_bwd_tc(const AttnParams& p, const float* lse, const void* dout, void* dq, void* dkn,
                                void* dv, const float* D, float* dkr_acc, const int* tile_amax64,
                                const int* tile_amin64, cudaStream_t stream);
+
+// Compressed-latent ragged attention (attn_latent.cu).  Expanded path: per-head
+// k_nope / v written from the latents (any dims, fp32 or bf16).  Absorbed path
+// (bf16 Kimi K3 MLA dims, kv_lora_rank 512, decode-shaped requests): q
+// absorption GEMM, latent attention with split-context partials, combine, and
+// the output projection GEMM, all in the workspace.
+size_t latent_expand_bytes(int H, int dn, int dv, int total_kv, bool bf16);
+cudaError_t launch_latent_expand(const void* c_kv, const void* w, bool bf16, int total_kv, int H, int dn, int dv,
+                                 int rank, void* kn_out, void* v_out, cudaStream_t stream);
+bool latent_absorbed_supported(int H, int dn, int dr, int dv, int rank, int max_q_len);
+size_t latent_absorbed_bytes(int R, int H, int total_q, int total_kv);
+cudaError_t launch_latent_absorbed(const AttnParams& p, const void* c_kv, const void* w, void* ws,
+                                   cudaStream_t stream);
 
 cudaError_t launch_build_mask(const int32_t* anchors, bool bf16, int B, int S, int Q, int nb, int bs, void* mask,
                               unsigned* err, cudaStream_t stream);

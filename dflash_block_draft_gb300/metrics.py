@@ -73,3 +73,26 @@ def ragged_work(q_offsets, kv_offsets, anchors, H, block_size, d_nope, d_rope, d
               + (qo.size + ko.size + an.size) * 4 + (H * total_q * 4 if lse else 0))
     return dict(pairs=pairs * H, flops=pairs * H * flops_per_pair(d_nope, d_rope, d_v), bytes=nbytes,
                 keys_read=keys)
+
+
+def latent_flops_per_pair(kv_rank: int, d_rope: int) -> int:
+    """Compressed-latent attention in absorbed form: the score over the latent
+    and the rope key, 2*(kv_rank + d_rope), and the latent output, 2*kv_rank,
+    per visible (query row, key, head)."""
+    return 2 * (kv_rank + d_rope) + 2 * kv_rank
+
+
+def latent_work(q_offsets, kv_offsets, anchors, H, block_size, d_nope, d_rope, d_v, kv_rank, esize=2):
+    """Work of the compressed-latent ragged call: the attention over the latents
+    (latent_flops_per_pair per visible pair) plus the query absorption and the
+    output projection, 2*d_nope*kv_rank and 2*kv_rank*d_v per (row, head).
+    Bytes: q once, the latent and rope key of every key some row sees once (not
+    per head), the projection weight once, out once."""
+    w = ragged_work(q_offsets, kv_offsets, anchors, H, block_size, d_nope, d_rope, d_v, esize=esize)
+    pairs = w["pairs"]
+    total_q = int(np.asarray(q_offsets)[-1])
+    flops = pairs * latent_flops_per_pair(kv_rank, d_rope) + total_q * H * 2 * kv_rank * (d_nope + d_v)
+    qo, ko, an = (np.asarray(x, np.int64) for x in (q_offsets, kv_offsets, anchors))
+    nbytes = (total_q * H * (d_nope + d_rope) * esize + w["keys_read"] * (kv_rank + d_rope) * esize
+              + H * (d_nope + d_v) * kv_rank * esize + total_q * H * d_v * esize + (qo.size + ko.size + an.size) * 4)
+    return dict(pairs=pairs, flops=flops, bytes=nbytes, keys_read=w["keys_read"])

@@ -161,6 +161,47 @@ DFLASH_API dflash_status_t dflash_attn_ragged(int R, int H, int d_nope, int d_ro
                                    dflash_stream_t stream);
 
 /*
+ * Ragged entry point over compressed KV latents (Kimi K3 MLA).  Each token
+ * carries its KV latent c (kv_rank values, after the latent norm) and the
+ * head-shared rope key; kv_b_proj expands the latent to one k_nope + v slice
+ * per head (nemo_automodel.components.speculative.dflash.draft_kimi_k3 page,
+ * KimiK3DFlashAttention: kv_b_proj produces num_attention_heads slices of
+ * qk_nope_head_dim + v_head_dim; ...dspark.draft_kimi_k3 page,
+ * KimiK3DSparkAttention: kv_lora_rank, kv_b_proj; nemo_automodel.components.
+ * models.kimi_k3.model page: the compressed latent is kv_lora_rank +
+ * qk_rope_head_dim values per token).  With w_kv_b viewed as [H, d_nope + d_v,
+ * kv_rank] (per head: the d_nope key rows, then the d_v value rows):
+ *   k_nope[t,h,e] = sum_c w_kv_b[h,e,c] c_kv[t,c],
+ *   v[t,h,e]      = sum_c w_kv_b[h,d_nope+e,c] c_kv[t,c],
+ * and the result is dflash_attn_ragged over those keys and values (same
+ * offsets, anchors, block rule, scale, out and lse).
+ *   q [total_q, H, d_nope+d_rope], c_kv [total_kv, kv_rank],
+ *   k_rope [total_kv, d_rope], w_kv_b [H, d_nope+d_v, kv_rank] (the
+ *   projection weight, row-major), out [total_q, H, d_v], lse [H, total_q].
+ * bf16 with (d_nope, d_rope, d_v, kv_rank) = (128, 64, 128, 512), H a multiple
+ * of 4 and max_q_len <= 16 (the serving decode shape) runs absorbed on the
+ * tensor cores: W_UK is folded into q, the attention runs over the latents
+ * (every head reads each token's latent once), and W_UV is applied after the
+ * softmax; q_abs and o_lat are rounded to bf16 on the way.  Every other shape
+ * (and fp32) expands the keys and values into the workspace and runs the
+ * ragged kernels on them.  A request skipped for invalid offsets or q_len >
+ * max_q_len is recorded as DFLASH_ERR_INVALID; its rows are written as 0
+ * (lse -inf) on the absorbed path and left unwritten on the expanded path.
+ *   workspace: >= dflash_attn_latent_workspace_size(...) bytes, 256-byte
+ *   aligned; needs no initialisation.
+ */
+#define DFLASH_MAX_KV_RANK 1024
+DFLASH_API size_t dflash_attn_latent_workspace_size(int R, int H, int d_nope, int d_rope, int d_v, int kv_rank,
+                                                    dflash_dtype_t dtype, int total_q, int total_kv, int max_q_len);
+DFLASH_API dflash_status_t dflash_attn_latent_ragged(int R, int H, int d_nope, int d_rope, int d_v, int kv_rank,
+                                                     float scale, dflash_dtype_t dtype, const void* q,
+                                                     const void* c_kv, const void* k_rope, const void* w_kv_b,
+                                                     const int32_t* q_offsets, const int32_t* kv_offsets,
+                                                     const int32_t* anchors, int block_size, int total_q,
+                                                     int total_kv, int max_q_len, void* out, float* lse,
+                                                     void* workspace, size_t ws_bytes, dflash_stream_t stream);
+
+/*
  * Dense entry point that allocates nothing and takes no workspace.  (No
  * counterpart on the pages: this is a convenience of this library.)
  *

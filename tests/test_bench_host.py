@@ -82,3 +82,16 @@ def test_committed_traffic_entries_name_existing_sources():
     for key, t in entries.items():
         assert os.path.exists(os.path.join(bench.ROOT, t["source"])), key
         assert len(t["source_md5"]) == 32 and t["bytes_per_launch"] > 0
+
+
+def test_latent_work_counts():
+    d = synth.make("decode_latent_bf16", R=3, H=4, ctx_lo=10, ctx_hi=300)
+    w = metrics.latent_work(d["q_offsets"], d["kv_offsets"], d["anchors"], 4, 16, 128, 64, 128, 512)
+    r = metrics.ragged_work(d["q_offsets"], d["kv_offsets"], d["anchors"], 4, 16, 128, 64, 128)
+    assert w["pairs"] == r["pairs"] and w["keys_read"] == r["keys_read"]
+    assert metrics.latent_flops_per_pair(512, 64) == 2 * 576 + 2 * 512
+    tq = d["total_q"]
+    assert w["flops"] == r["pairs"] * 2176 + tq * 4 * 2 * 512 * 256
+    # per key 1152 bytes of latent + rope key instead of 4 heads x 512 + 128 expanded bytes
+    expect = tq * 4 * 192 * 2 + r["keys_read"] * 576 * 2 + 4 * 256 * 512 * 2 + tq * 4 * 128 * 2 + (4 + 4 + tq // 16) * 4
+    assert w["bytes"] == expect
