@@ -275,12 +275,15 @@ cudaError_t launch_head_gemm(const GemmArgs& g, const CUtensorMap& mA, const CUt
 // TMEM lane quarter (keys 32q..32q+31), each owning 32 of the 64 rows.  The
 // control warpgroup gives registers back (setmaxnreg 104) so that the softmax
 // warps get 200: 128*104 + 256*200 = 384*168, the launch budget.
-// Shared memory: Q^T (9 panels of 64 rows x 64 dims), and one key tile as 9
-// slots of 128 keys x 64 dims (8 latent panels, then the rope panel).  Once
-// QK of a tile has completed its rope slot is free, and the softmax writes
-// P^T there (64 rows x 128 keys, bf16, two K-major panels); PV reads the
-// latent slots as V^T (MN-major) and P^T, and each slot is refilled with the
-// next tile's panel as soon as the MMAs reading it complete.
+// Shared memory: Q^T (9 panels of 64 rows x 64 dims), one key tile as 9 slots
+// of 128 keys x 64 dims (8 latent panels, then the rope panel), and one 8 KB
+// P^T panel (64 rows x 64 keys, bf16, K-major).  PV runs in two key halves
+// through that panel: the softmax warps of keys 0-63 write it, PV of those
+// keys goes out for all four latent blocks, then the warps of keys 64-127
+// overwrite it and the second half goes out.  The rope slot is therefore free
+// as soon as QK of a tile completes, and the next tile's rope panel loads
+// while this tile's softmax and PV run; each latent slot is refilled as soon
+// as the second-half PV reading it completes.
 // TMEM: S^T [0,64) (128 keys x 64 rows), O^T blocks [64 + 64m, +64), m < 4
 // (128 latent dims x 64 rows each).
 // ============================================================================
@@ -293,15 +296,18 @@ constexpr uint32_t kLQPanel = kLRows * 128;     // 8 KB
 constexpr uint32_t kLKPanel = kLBN * 128;       // 16 KB
 constexpr uint32_t kLOffQ = 0;
 constexpr uint32_t kLOffK = kLPanels * kLQPanel;
-constexpr uint32_t kLOffBar = kLOffK + kLPanels * kLKPanel;
+constexpr uint32_t kLOffP = kLOffK + kLPanels * kLKPanel;
+constexpr uint32_t kLOffBar = kLOffP + kLQPanel;
 enum {
   LB_Q_FULL = 0,
   LB_Q_EMPTY = 1,
   LB_SLOT_FULL = 2,
   LB_SLOT_EMPTY = LB_SLOT_FULL + kLPanels,
   LB_S_FULL = LB_SLOT_EMPTY + kLPanels,
-  LB_P_FULL = LB_S_FULL + 1,   // 256 arrivals: P^T written
-  LB_PV_DONE = LB_P_FULL + 1,  // one phase per tile
+  LB_P_LO = LB_S_FULL + 1,     // 128 arrivals: P^T of keys 0-63 written
+  LB_P_FREE = LB_P_LO + 1,     // first-half PV issued and complete: the P^T panel may be overwritten
+  LB_P_HI = LB_P_FREE + 1,     // 128 arrivals: P^T of keys 64-127 written
+  LB_PV_DONE = LB_P_HI + 1,    // one phase per tile
   LB_O_FULL = LB_PV_DONE + 1,
   LB_DRAIN = LB_O_FULL + 1,
   kLBars = LB_DRAIN + 1
@@ -309,7 +315,7 @@ enum {
 constexpr uint32_t kLOffSlot = kLOffBar + 8 * kLBars;
 constexpr uint32_t kLOffAbort = kLOffSlot + 4;
 constexpr uint32_t kLOffRed = kLOffAbort + 12;
-constexpr uint32_t kLRedWords = 4 * kLRows + 9 + kLTok;  // maxima/sums [4][64], vote [3][3], anchors [16]
+constexpr uint32_t kLRedWords = 4 * kLRows + 9 + 3 * kLTok;  // maxima/sums [4][64], vote [3][3], token bounds [3][16]
 constexpr uint32_t kLSmem = kLOffRed + 4 * kLRedWords + 1024;
 static_assert(kLSmem <= 232448, "shared memory budget");
 constexpr uint32_t kLTmemCols = 512;
@@ -379,6 +385,9 @@ __device__ __forceinline__ int lnext_tile(const LatentArgs& a, const LUnit& it, 
   return it.kt1;
 }
 
+// Load order of a key tile's panels: the rope slot first, then latent 0..7.
+__device__ __forceinline__ int lslot_of(int i) { return i == 0 ? kLPanels - 1 : i - 1; }
+
 __global__ void __launch_bounds__(kLThreads, 1)
     latent_attn_kernel(const __grid_constant__ LatentArgs a, const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR) {
@@ -397,7 +406,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kLOffSlot);
   float* red = reinterpret_cast<float*>(smem + kLOffRed);                // [4][64]
   unsigned* vote = reinterpret_cast<unsigned*>(red + 4 * kLRows);        // [3][3]
-  int* s_ctx = reinterpret_cast<int*>(vote + 9);                         // [16]
+  int* s_ctx = reinterpret_cast<int*>(vote + 9);                         // [3][16]: anchor, block lo, hi
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ctl.bar(LB_Q_FULL), 1);
@@ -407,7 +416,9 @@ __global__ void __launch_bounds__(kLThreads, 1)
       ptx::mbar_init(ctl.bar(LB_SLOT_EMPTY + s), 1);
     }
     ptx::mbar_init(ctl.bar(LB_S_FULL), 1);
-    ptx::mbar_init(ctl.bar(LB_P_FULL), 256);
+    ptx::mbar_init(ctl.bar(LB_P_LO), 128);
+    ptx::mbar_init(ctl.bar(LB_P_FREE), 1);
+    ptx::mbar_init(ctl.bar(LB_P_HI), 128);
     ptx::mbar_init(ctl.bar(LB_PV_DONE), 1);
     ptx::mbar_init(ctl.bar(LB_O_FULL), 1);
     ptx::mbar_init(ctl.bar(LB_DRAIN), 1);
@@ -448,7 +459,9 @@ __global__ void __launch_bounds__(kLThreads, 1)
         if ((int)blockIdx.x == p.stall_cta) break;  // timeout test: this unit's key tiles never arrive
         for (int kt = lnext_tile(a, it, it.kt0 - 1); kt < it.kt1 && !stop; kt = lnext_tile(a, it, kt)) {
           const int krow = (int)(it.sg.kv0 + (long long)kt * kLBN);
-          for (int pn = 0; pn < kLPanels; ++pn) {
+          // the rope panel first: its slot is freed by QK, the latent slots only by PV
+          for (int ip = 0; ip < kLPanels; ++ip) {
+            const int pn = lslot_of(ip);
             const uint32_t tile = pc / kLPanels;
             if (!ctl.wait(LB_SLOT_EMPTY + pn, (tile & 1u) ^ 1u)) {
               stop = true;
@@ -465,7 +478,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
       // Wind-down: the outstanding loads (the last kLPanels panels, the last Q)
       // land before the CTA exits.
       for (uint32_t i = pc > (uint32_t)kLPanels ? pc - kLPanels : 0u; i < pc; ++i)
-        ctl.wait_landed(LB_SLOT_FULL + i % kLPanels, (i / kLPanels) & 1u);
+        ctl.wait_landed(LB_SLOT_FULL + lslot_of((int)(i % kLPanels)), (i / kLPanels) & 1u);
       if (n > 0) ctl.wait_landed(LB_Q_FULL, (n - 1) & 1u);
     }
   } else if (warp == 1) {
@@ -501,27 +514,39 @@ __global__ void __launch_bounds__(kLThreads, 1)
           }
           if (stop) break;
           ptx::tc_commit(ctl.bar(LB_S_FULL));
+          ptx::tc_commit(ctl.bar(LB_SLOT_EMPTY + kLPanels - 1));  // the rope slot: read by QK only
           if (kn >= it.kt1) ptx::tc_commit(ctl.bar(LB_Q_EMPTY));  // every QK of this unit issued
-          // O^T += V^T P^T, latent block by latent block; a block's two slots are
-          // released as soon as its MMAs complete.
-          if (!ctl.wait(LB_P_FULL, g & 1u)) {
+          // O^T += V^T P^T in two key halves through the one P^T panel; a latent
+          // block's two slots are released as soon as its second half completes.
+          const uint32_t sP = sbase + kLOffP;
+          if (!ctl.wait(LB_P_LO, g & 1u)) {
             stop = true;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sP = sK + (kLPanels - 1) * kLKPanel;
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
 #pragma unroll
-            for (int ks = 0; ks < kLBN / 16; ++ks)
+            for (int ks = 0; ks < 4; ++ks)
               ptx::mma_ss(tmem + kLColO + 64u * m, ptx::smem_desc(sK + 2 * m * kLKPanel + ks * 2048, kLKPanel, 1024),
-                          ptx::smem_desc(sP + (ks >> 2) * kLQPanel + (ks & 3) * 32, 16, 1024), kLIdPV,
-                          !(first && ks == 0));
+                          ptx::smem_desc(sP + ks * 32, 16, 1024), kLIdPV, !(first && ks == 0));
+          }
+          ptx::tc_commit(ctl.bar(LB_P_FREE));
+          if (!ctl.wait(LB_P_HI, g & 1u)) {
+            stop = true;
+            break;
+          }
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m) {
+#pragma unroll
+            for (int ks = 4; ks < 8; ++ks)
+              ptx::mma_ss(tmem + kLColO + 64u * m, ptx::smem_desc(sK + 2 * m * kLKPanel + ks * 2048, kLKPanel, 1024),
+                          ptx::smem_desc(sP + (ks - 4) * 32, 16, 1024), kLIdPV, 1u);
             ptx::tc_commit(ctl.bar(LB_SLOT_EMPTY + 2 * m));
             ptx::tc_commit(ctl.bar(LB_SLOT_EMPTY + 2 * m + 1));
           }
           ptx::tc_commit(ctl.bar(LB_PV_DONE));
-          ptx::tc_commit(ctl.bar(LB_SLOT_EMPTY + kLPanels - 1));
           first = false;
           ++g;
           if (kn >= it.kt1) break;
@@ -548,8 +573,20 @@ __global__ void __launch_bounds__(kLThreads, 1)
       const LUnit it = latent_unit(a, u);
       if (!it.ok) continue;
       const int S = it.sg.S, Qn = it.sg.Q, K = S + Qn;
-      if (st < kLTok) s_ctx[st] = st < Qn ? row_anchor(p, it.sg, st) : 0;
+      if (st < kLTok) {
+        // per draft token: its anchor, and its own block's noise keys [lo, hi)
+        const int blk = st / p.bs;
+        s_ctx[st] = st < Qn ? row_anchor(p, it.sg, st) : 0;
+        s_ctx[kLTok + st] = S + blk * p.bs;
+        s_ctx[2 * kLTok + st] = S + min(blk * p.bs + p.bs, Qn);
+      }
       ptx::named_barrier(kLSoftBar, 256);
+      // This thread's 32 rows are the 4 heads of draft tokens 8hf .. 8hf+7: the
+      // visibility of its key is decided once per token and spread over the 4 rows.
+      uint32_t rows_valid = 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (8 * hf + u < Qn) rows_valid |= 0xFu << (4 * u);
       float m_ref[32], l_part[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
@@ -569,16 +606,18 @@ __global__ void __launch_bounds__(kLThreads, 1)
           ptx::tc_fence_after();
           ptx::tmem_ld32(tmem + lane_off + kLColS + 32u * hf, reinterpret_cast<uint32_t*>(x));
           ptx::tmem_wait_ld();
+          uint32_t vmask = rows_valid;
+          if (!full) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int t = 8 * hf + u;
+              const bool v = key < s_ctx[t] || (key >= s_ctx[kLTok + t] && key < s_ctx[2 * kLTok + t]);
+              if (!v) vmask &= ~(0xFu << (4 * u));
+            }
+          }
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const int t = (32 * hf + c) >> 2;  // draft token of row 32hf + c
-            bool vis = t < Qn;
-            if (!full && vis) {
-              const int blk = t / p.bs;
-              const int nlo = S + blk * p.bs, nhi = S + min(blk * p.bs + p.bs, Qn);
-              vis = key < s_ctx[t] || (key >= nlo && key < nhi);
-            }
-            x[c] = vis ? x[c] * c2 : -INFINITY;
+            x[c] = (vmask >> c) & 1u ? x[c] * c2 : -INFINITY;
             if (x[c] > m_ref[c] + 8.0f) flags |= 1u << c;
           }
         }
@@ -647,20 +686,31 @@ __global__ void __launch_bounds__(kLThreads, 1)
           }
           ptx::named_barrier(kLSoftBar, 256);  // red[] is free again
         }
-        // p = exp2(x - m_ref); P^T[row][key] in the rope slot, 128-byte-swizzled K-major
-        uint8_t* pt = smem + kLOffK + (kLPanels - 1) * kLKPanel + (kin >> 6) * kLQPanel;
+        // p = exp2(x - m_ref), as bf16; then P^T[row][key] into the P^T panel
+        // (128-byte-swizzled K-major): keys 0-63 first, keys 64-127 once PV of
+        // the first half has completed.
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float p0 = m_ref[c] == -INFINITY ? 0.f : ptx::ex2(x[c] - m_ref[c]);
+          const float p1 = m_ref[c + 1] == -INFINITY ? 0.f : ptx::ex2(x[c + 1] - m_ref[c + 1]);
+          l_part[c] += p0;
+          l_part[c + 1] += p1;
+          pk[c / 2] = ptx::pack_bf16x2(p0, p1);
+        }
+        const bool hi_keys = kin >= 64;  // warp-uniform: quarters 2 and 3
+        if (hi_keys) ctl.wait(LB_P_FREE, g & 1u);
+        uint8_t* pt = smem + kLOffP;
         const int cb = (kin & 63) * 2;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int r = 32 * hf + c;
-          const float pv = m_ref[c] == -INFINITY ? 0.f : ptx::ex2(x[c] - m_ref[c]);
-          l_part[c] += pv;
-          *reinterpret_cast<__nv_bfloat16*>(pt + r * 128 + ((((cb >> 4) ^ (r & 7))) << 4) + (cb & 15)) =
-              __float2bfloat16_rn(pv);
+          *reinterpret_cast<uint16_t*>(pt + r * 128 + ((((cb >> 4) ^ (r & 7))) << 4) + (cb & 15)) =
+              (uint16_t)(pk[c / 2] >> (16 * (c & 1)));
         }
         ptx::fence_proxy_async_smem();  // P^T written by threads, read by the tensor core
         ptx::tc_fence_before();
-        ptx::mbar_arrive(ctl.bar(LB_P_FULL));
+        ptx::mbar_arrive(ctl.bar(hi_keys ? LB_P_HI : LB_P_LO));
         first = false;
       }
       if (stop) break;
