@@ -608,7 +608,7 @@ def measure_latent(dfl, steps, warmup, device, world, peaks, requests=None):
             "steps": steps, "gbs": work["bytes"] / (kernel_ms / 1e3) / 1e9,
             "unmasked_flops_per_step": work["flops"], "algorithmic_bytes_per_step": work["bytes"],
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak,
+                         "frac": achieved / peak, "traffic": load_traffic("decode_latent_bf16", work["bytes"]),
                          "kernel": "q absorption GEMM + split plan + latent attention + merge + output projection GEMM",
                          "flops_note": "2*(kv_rank+d_rope) + 2*kv_rank per visible (row, key, head), plus "
                                        "2*kv_rank*(d_nope+d_v) per (row, head)"},
