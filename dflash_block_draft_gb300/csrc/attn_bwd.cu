@@ -477,6 +477,7 @@ cudaError_t launch_tiles(const BwdArgs& a, size_t smem, cudaStream_t stream) {
 bool use_bwd_tc(const AttnParams& p, bool bf16) {
   if (!bf16 || !bwd_tc_supported(p.dn, p.dr, p.dv)) return false;
   if ((long long)p.B * p.Q + 128 >= (1ll << 31) || (long long)p.B * (p.S + p.Q) + 128 >= (1ll << 31)) return false;
+  if ((long long)p.H * p.B * (((long long)p.S + p.Q + 127) / 128) >= (1ll << 31)) return false;  // 1-D grid
   const char* v = getenv("DFLASH_FORCE_SIMT");
   return !(v && v[0] && v[0] != '0');
 }

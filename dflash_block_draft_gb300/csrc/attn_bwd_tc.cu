@@ -45,6 +45,8 @@
 // records DFLASH_ERR_TIMEOUT and the CTA winds down.
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -104,7 +106,28 @@ struct BwdTcArgs {
   const int* tile_amin;  // [B, ceil(Q/64)] smallest anchor of each 64-row query tile
   int nqt64;
   int mask_vec;  // dense: 16-byte mask loads allowed
+  int group;     // (batch row, head) pairs per scheduling group
 };
+
+// CTA order.  CTAs are dispatched in linear block order; the grid is 1-D over
+// groups of `group` (batch row, head) pairs, and inside a group over tile levels
+// longest first with the pairs fastest.  Inside a group the longest tiles start
+// first (tails are filled by short ones); the group keeps the K/V streams that
+// are live at once few enough to stay in L2.  group = 0 keeps the plain order
+// (tiles fastest, in index order), which measured faster with dense masks.
+// Returns (level, pair); level 0 is the longest tile.
+__device__ __forceinline__ int2 cta_place(int group, int ntiles, int zh, bool last_first) {
+  const long long L = blockIdx.x;
+  if (group == 0) {
+    const int tile = (int)(L % ntiles);
+    return make_int2(last_first ? ntiles - 1 - tile : tile, (int)(L / ntiles));
+  }
+  const long long per = (long long)group * ntiles;
+  const int grp = (int)(L / per);
+  const int g0 = grp * group, gsz = min(group, zh - g0);
+  const int r = (int)(L - grp * per);
+  return make_int2(r / gsz, g0 + r % gsz);
+}
 
 __device__ __forceinline__ int clamp_anchor(const AttnParams& p, long long idx) {
   int a = p.anchors[idx];
@@ -217,7 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Smem s = setup_smem(smem_raw, p.err);
   const Ctl& ctl = s.ctl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // The last query tiles first: under sorted anchors they see the most context.
+  const int nqt128 = (p.Q + 127) / 128;
+  const int2 pl = cta_place(a.group, nqt128, p.H * p.B, true);
+  const int t = nqt128 - 1 - pl.x, h = pl.y % p.H, b = pl.y / p.H;
   const int S = p.S, Q = p.Q, K = S + Q;
   const int r0 = t * 128, r1 = min(r0 + 128, Q);
   const int nkt = (K + 63) / 64;
@@ -440,7 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Smem s = setup_smem(smem_raw, p.err);
   const Ctl& ctl = s.ctl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // The first key tiles first: under sorted anchors the most query rows see them.
+  const int2 pl = cta_place(a.group, (p.S + p.Q + 127) / 128, p.H * p.B, false);
+  const int kt = pl.x, h = pl.y % p.H, b = pl.y / p.H;
   const int S = p.S, Q = p.Q, K = S + Q;
   const int k0 = kt * 128, k1 = min(k0 + 128, K);
   const int nqt = a.nqt64;
@@ -762,12 +790,23 @@ cudaError_t launch_attn_bwd_tc(const AttnParams& p, const float* lse, const void
   if (e != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) != cudaSuccess)
     return e;
+  // Scheduling groups of about three waves of CTAs each.
+  const int nsm = sm_count() > 0 ? sm_count() : 148;
+  const int zh = p.H * p.B;
+  auto group_for = [&](int ntiles) {
+    const long long ng = std::max(1LL, ((long long)zh * ntiles + 3LL * nsm / 2) / (3LL * nsm));  // groups, rounded
+    return (int)((zh + ng - 1) / ng);
+  };
   if (p.Q > 0) {
-    kdq<<<dim3((p.Q + 127) / 128, p.H, p.B), kThreads, kSmemBytes, stream>>>(a, q128, do128, kn64, kr64, v64);
+    const int nq = (p.Q + 127) / 128;
+    a.group = dense ? 0 : group_for(nq);
+    kdq<<<(unsigned)((long long)zh * nq), kThreads, kSmemBytes, stream>>>(a, q128, do128, kn64, kr64, v64);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  kkv<<<dim3((p.S + p.Q + 127) / 128, p.H, p.B), kThreads, kSmemBytes, stream>>>(a, q64, do64, kn128, kr128, v128);
+  const int nk = (p.S + p.Q + 127) / 128;
+  a.group = dense ? 0 : group_for(nk);
+  kkv<<<(unsigned)((long long)zh * nk), kThreads, kSmemBytes, stream>>>(a, q64, do64, kn128, kr128, v128);
   count_launch();
   return cudaGetLastError();
 }
