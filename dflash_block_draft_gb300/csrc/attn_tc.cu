@@ -126,6 +126,7 @@ struct TcArgs {
   int n_items;  // npair * segments * H
   int mask_vec; // dense: mask rows are 16-byte aligned
   int out_v8;   // out is 32-byte aligned: rows are written with 32-byte stores
+  int cls_v16;  // dense: every row of tile classes starts 16-byte aligned
 };
 
 struct Item {
@@ -209,8 +210,23 @@ __device__ __forceinline__ int next_tile(const TcArgs& a, const Item& it, int kt
     kt = max(kt, it.noise_begin);
     return kt < it.noise_end ? kt : it.nkt;
   }
+  // SKIP is 0, so a run of skipped tiles is a run of zero bytes in both halves'
+  // class rows: look at 16 tiles per load once the index is 16-aligned (a tile
+  // at a time would cost one dependent load per skipped tile).
+  const uint8_t* c0 = it.cls[0];
+  const uint8_t* c1 = it.has[1] ? it.cls[1] : it.cls[0];
+  for (; kt < it.nkt && (!a.cls_v16 || (kt & 15)); ++kt)
+    if ((__ldg(c0 + kt) | __ldg(c1 + kt)) != DFLASH_TILE_SKIP) return kt;
+  for (; kt + 16 <= it.nkt; kt += 16) {
+    const uint4 w0 = __ldg(reinterpret_cast<const uint4*>(c0 + kt));
+    const uint4 w1 = __ldg(reinterpret_cast<const uint4*>(c1 + kt));
+    const uint32_t w[4] = {w0.x | w1.x, w0.y | w1.y, w0.z | w1.z, w0.w | w1.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (w[u]) return kt + 4 * u + (__ffs(w[u]) - 1) / 8;
+  }
   for (; kt < it.nkt; ++kt)
-    if (it.cls[0][kt] != DFLASH_TILE_SKIP || (it.has[1] && it.cls[1][kt] != DFLASH_TILE_SKIP)) return kt;
+    if ((__ldg(c0 + kt) | __ldg(c1 + kt)) != DFLASH_TILE_SKIP) return kt;
   return it.nkt;
 }
 
@@ -730,6 +746,8 @@ cudaError_t launch_attn_tc(const AttnParams& p, int segments, int nqt, long long
   a.mask_vec = 0;
   if (p.mode == kDense) a.mask_vec = (((uintptr_t)p.mask & 15u) == 0) && ((p.S + p.Q) % 8 == 0);
   a.out_v8 = ((uintptr_t)p.out & 31u) == 0;
+  // class rows are nkt bytes apart from a 16-byte aligned base (the workspace)
+  a.cls_v16 = p.mode == kDense && ((uintptr_t)p.classes & 15u) == 0 && p.nkt % 16 == 0;
   if (a.n_items <= 0) return cudaSuccess;
   CUtensorMap mq, mkn, mkr, mv;
   if (!make_map_3d(&mq, p.q, q_rows, p.H, kDn + kDr, kBM) || !make_map_3d(&mkn, p.kn, kv_rows, p.H, kDn, kBN) ||
