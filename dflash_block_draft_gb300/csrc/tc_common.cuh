@@ -95,6 +95,9 @@ __device__ __forceinline__ uint64_t range_bits(int lo, int hi) {
 // Applies the row's mask to the 64 scores of tile columns [c0, c0+64) in place:
 // FULL leaves raw scores, anchored sets hidden keys to -inf (raw scores stay
 // raw), dense turns scores into base-2 units plus the mask, NONE sets all -inf.
+// DENSE selects the mask kind at compile time, so that each kernel carries only
+// its own masking code (the softmax loop is instruction-cache bound).
+template <bool DENSE>
 __device__ __forceinline__ void mask64(float* x, int kind, int c0, const PrepCtx& pc) {
   if (kind == kPrepFull) return;
   if (kind == kPrepNone) {
@@ -102,7 +105,7 @@ __device__ __forceinline__ void mask64(float* x, int kind, int c0, const PrepCtx
     for (int c = 0; c < 64; ++c) x[c] = -INFINITY;
     return;
   }
-  if (kind == kPrepAnchored) {
+  if (!DENSE) {
     // visible: c < c_ctx (context below the anchor) or c_lo <= c < c_hi (own block)
     const uint64_t vis = range_bits(0, pc.c_ctx - c0) | range_bits(pc.c_lo - c0, pc.c_hi - c0);
     const uint32_t lo = (uint32_t)vis, hi = (uint32_t)(vis >> 32);
