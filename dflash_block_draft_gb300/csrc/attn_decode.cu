@@ -64,7 +64,7 @@ enum {
 constexpr uint32_t kOffTmemSlot = kOffBar + 8 * kNumBars;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
 constexpr uint32_t kOffRed = kOffAbort + 12;               // softmax scratch (floats)
-constexpr uint32_t kRedFloats = 4 * kQN + 3 + kQN;         // per-warp maxima/sums, vote words, anchors
+constexpr uint32_t kRedFloats = 4 * kQN + 3 + 3 * kQN;     // per-warp maxima/sums, vote words, row key bounds
 constexpr uint32_t kSmemBytes = kOffRed + 4 * kRedFloats + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -156,7 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
   float* red = reinterpret_cast<float*>(smem + kOffRed);  // [4][kQN] per-warp values
   unsigned* vote = reinterpret_cast<unsigned*>(red + 4 * kQN);  // [3] vote words, used in rotation
-  int* s_ctx = reinterpret_cast<int*>(red + 4 * kQN + 3);        // [kQN] anchors of the rows
+  // [3][kQN] per row: anchor (context keys below it are visible), first and
+  // one-past-last key of the row's own noise block
+  int* s_ctx = reinterpret_cast<int*>(red + 4 * kQN + 3);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ctl.bar(BAR_Q_FULL), 1);
@@ -324,7 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit it = decode_unit(a, u);
       if (!it.ok) continue;
       const int S = it.sg.S, Qn = it.sg.Q, K = S + Qn;
-      if (st < kQN) s_ctx[st] = st < Qn ? row_anchor(p, it.sg, st) : 0;
+      if (st < kQN) {
+        const int blk = st / p.bs;
+        s_ctx[st] = st < Qn ? row_anchor(p, it.sg, st) : 0;
+        s_ctx[kQN + st] = st < Qn ? S + blk * p.bs : 0;
+        s_ctx[2 * kQN + st] = st < Qn ? S + min(blk * p.bs + p.bs, Qn) : 0;
+      }
       ptx::named_barrier(kSoftmaxBarrier, 128);
       float m_ref[kQN], l_part[kQN];
 #pragma unroll
@@ -348,11 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < kQN; ++q) {
           bool vis = full ? q < Qn : false;
-          if (!full && q < Qn) {
-            const int blk = q / p.bs;
-            const int nlo = S + blk * p.bs, nhi = S + min(blk * p.bs + p.bs, Qn);
-            vis = key < s_ctx[q] || (key >= nlo && key < nhi);
-          }
+          if (!full && q < Qn) vis = key < s_ctx[q] || (key >= s_ctx[kQN + q] && key < s_ctx[2 * kQN + q]);
           x[q] = vis ? x[q] * c2 : -INFINITY;
           if (x[q] > m_ref[q] + 8.0f) flags |= 1u << q;
         }
