@@ -39,7 +39,10 @@ namespace {
 constexpr int kDn = 128, kDr = 64, kDv = 128;
 constexpr int kBN = 128;            // keys per tile
 constexpr int kQN = 16;             // query rows per request (MMA N)
-constexpr int kSplitTiles = 16;     // tiles per work unit (2048 keys)
+// Tiles per work unit (4096 keys).  Each unit pays a Q load, a pipeline fill and
+// an epilogue; 16, 24, 32, 48 and 64 tiles measured 76, 80, 82, 79 and 79 % of
+// the HBM peak on the decode workload (longer units leave a longer tail).
+constexpr int kSplitTiles = 32;
 constexpr uint32_t kPanel = 128 * 128;      // K/V panel: 128 rows x 128 bytes
 constexpr uint32_t kQPanel = kQN * 128;     // Q / P^T panel: 16 rows x 128 bytes
 constexpr uint32_t kRing = 10;

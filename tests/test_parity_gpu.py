@@ -286,7 +286,7 @@ def test_ragged_decode_shape_small(dfl, kernel):
 @pytest.mark.parametrize("bs,nb,seed", [(16, 1, 81), (8, 2, 82), (4, 4, 83)])
 def test_ragged_decode_split_context_every_row(dfl, bs, nb, seed):
     # 16 draft rows per request (split-context kernels), contexts that cross the
-    # 2048-key split boundaries, anchors anywhere in [0, S_r]
+    # 4096-key split boundaries, anchors anywhere in [0, S_r]
     d = synth.make("decode_bf16", seed=seed, R=6, H=2, ctx_lo=1500, ctx_hi=9000, nb=nb, block_size=bs)
     rng = np.random.default_rng(seed)
     for r in range(6):
@@ -322,7 +322,7 @@ def test_ragged_mixed_lengths_every_row(dfl, dtype, dn, dr, dv, bs, q_blocks, ke
 @pytest.mark.parametrize("seed", [95, 96])
 def test_ragged_decode_mixed_lengths_split_context_every_row(dfl, seed):
     """The split-context decode path (max_q_len <= 16) with requests of 8 and 16
-    rows and contexts that cross the 2048-key split boundaries."""
+    rows and contexts that cross the 4096-key split boundaries."""
     d = synth.make("decode_bf16", seed=seed, R=8, H=2, ctx_lo=1500, ctx_hi=9000, block_size=8, q_blocks=(1, 2))
     assert set(np.diff(d["q_offsets"]).tolist()) == {8, 16}
     want_o, want_l = oracle.ragged(d["q"], d["k_nope"], d["k_rope"], d["v"], d["q_offsets"], d["kv_offsets"],
