@@ -57,7 +57,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # The rest of the suite, reported beside the headline: (workload, entry point).
 PER_CONFIG = (("prefill_bf16", "anchored"), ("prefill_bf16", "dense"), ("training_bf16", "anchored"),
               ("training_bf16", "dense"), ("long_bf16", "dense"), ("decode_bf16", "ragged"),
-              ("decode_latent_bf16", "latent"), ("tiny_fp32", "anchored"))
+              ("decode_latent_bf16", "latent"), ("prefill_bf16", "backward"), ("training_bf16", "backward"),
+              ("long_bf16", "backward"), ("tiny_fp32", "anchored"))
 # Targets: prefill-shaped workloads at >= 50 % of the bf16 tensor peak, the
 # ragged decode at >= 60 % of HBM bandwidth.
 TARGET_FRAC = {"tensor": 0.50, "hbm": 0.60}
@@ -669,6 +670,10 @@ def run_ours(args):
                 r = measure_decode(dfl, args.steps, args.warmup, device, 1, peaks)
             elif w == "decode_latent_bf16":
                 r = measure_latent(dfl, args.steps, args.warmup, device, 1, peaks)
+            elif mode == "backward":  # the anchored backward, given the forward's out and lse
+                dw = synth.make(w)
+                r = measure_batched(dfl, dw, "anchored", True, args.steps, args.warmup, device, 1, peaks)
+                del dw
             else:
                 dw = synth.make(w)
                 r = measure_batched(dfl, dw, mode, False, args.steps, args.warmup, device, 1, peaks,
