@@ -39,9 +39,12 @@ namespace {
 constexpr int kDn = 128, kDr = 64, kDv = 128;
 constexpr int kBN = 128;            // keys per tile
 constexpr int kQN = 16;             // query rows per request (MMA N)
-// Tiles per work unit (4096 keys).  Each unit pays a Q load, a pipeline fill and
-// an epilogue; 16, 24, 32, 48 and 64 tiles measured 76, 80, 82, 79 and 79 % of
-// the HBM peak on the decode workload (longer units leave a longer tail).
+// At most this many tiles per work unit (4096 keys): a request's context is cut
+// into ceil(tiles / kSplitTiles) splits of equal size (within one tile).  Each
+// unit pays a Q load, a pipeline fill and an epilogue, and longer units leave a
+// longer tail: limits of 16, 24, 32, 48 and 64 tiles measured 76, 80, 82, 79 and
+// 79 % of the HBM peak on the decode workload with full splits plus a remainder;
+// equal splits added 1 % at 32.
 constexpr int kSplitTiles = 32;
 constexpr uint32_t kPanel = 128 * 128;      // K/V panel: 128 rows x 128 bytes
 constexpr uint32_t kQPanel = kQN * 128;     // Q / P^T panel: 16 rows x 128 bytes
@@ -117,8 +120,10 @@ __device__ __forceinline__ Unit decode_unit(const DecodeArgs& a, int u) {
   it.ok = it.sg.ok && it.sg.Q <= kQN && w < a.max_slots;
   if (!it.ok) return it;
   const int nkt = (it.sg.S + it.sg.Q + kBN - 1) / kBN;
-  it.kt0 = it.s * kSplitTiles;
-  it.kt1 = min(nkt, it.kt0 + kSplitTiles);
+  // ceil(nkt / kSplitTiles) splits of equal size (within one tile)
+  const int nsplit = (nkt + kSplitTiles - 1) / kSplitTiles;
+  it.kt0 = (int)((long long)it.s * nkt / nsplit);
+  it.kt1 = (int)((long long)(it.s + 1) * nkt / nsplit);
   it.amin = it.sg.S;
   it.amax = 0;
   for (int j = 0; j <= (it.sg.Q - 1) / p.bs; ++j) {

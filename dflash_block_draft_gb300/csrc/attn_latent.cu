@@ -291,10 +291,13 @@ constexpr int kLRank = 512, kLDr = 64;
 constexpr int kLPanels = (kLRank + kLDr) / 64;  // 9
 constexpr int kLBN = 128;                       // keys per tile
 constexpr int kLHeads = 4, kLTok = 16, kLRows = kLHeads * kLTok;
-// Key tiles per unit (3584 keys): each unit pays a Q load, a pipeline fill and an
-// epilogue, longer units leave a longer tail; 24, 28, 32, 40, 48 and 64 tiles
-// measured 1.88, 1.80, 1.83, 1.95, 1.90 and 2.09 ms on the latent decode workload.
-constexpr int kLSplit = 28;
+// At most this many key tiles per unit (3072 keys): a request's context is cut
+// into ceil(tiles / kLSplit) splits of equal size (within one tile).  Each unit
+// pays a Q load, a pipeline fill and an epilogue, and longer units leave a longer
+// tail.  On the latent decode workload, full splits plus a remainder measured
+// 1.88, 1.80, 1.83, 1.95, 1.90 and 2.09 ms for 24, 28, 32, 40, 48 and 64 tiles;
+// equal splits 1.78, 1.75, 1.73, 1.75 and 1.74 ms for 16, 20, 24, 28 and 32.
+constexpr int kLSplit = 24;
 constexpr uint32_t kLQPanel = kLRows * 128;     // 8 KB
 constexpr uint32_t kLKPanel = kLBN * 128;       // 16 KB
 constexpr uint32_t kLOffQ = 0;
@@ -365,8 +368,10 @@ __device__ __forceinline__ LUnit latent_unit(const LatentArgs& a, int u) {
   it.ok = it.sg.ok && it.sg.Q <= kLTok && w < a.max_slots;
   if (!it.ok) return it;
   const int nkt = (it.sg.S + it.sg.Q + kLBN - 1) / kLBN;
-  it.kt0 = (w - a.prefix[lo]) * kLSplit;
-  it.kt1 = min(nkt, it.kt0 + kLSplit);
+  // ceil(nkt / kLSplit) splits of equal size (within one tile)
+  const int nsplit = (nkt + kLSplit - 1) / kLSplit, s = w - a.prefix[lo];
+  it.kt0 = (int)((long long)s * nkt / nsplit);
+  it.kt1 = (int)((long long)(s + 1) * nkt / nsplit);
   it.amin = it.sg.S;
   it.amax = 0;
   for (int j = 0; j <= (it.sg.Q - 1) / p.bs; ++j) {

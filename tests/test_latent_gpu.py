@@ -60,7 +60,7 @@ def test_expanded_path_general_dims_every_row(dfl, dtype):
 @pytest.mark.parametrize("bs,q_blocks,seed", [(16, (1,), 202), (8, (1, 2), 203), (4, (2, 4), 204)])
 def test_absorbed_path_decode_shape_every_row(dfl, bs, q_blocks, seed):
     """Kimi K3 MLA dims, kv_lora_rank 512, at most 16 rows per request; contexts
-    that cross the 3584-key split boundaries; anchors anywhere in [0, S_r]."""
+    that cross split boundaries (at most 3072 keys per split); anchors anywhere in [0, S_r]."""
     d = synth.make("decode_latent_bf16", seed=seed, R=6, H=8, ctx_lo=200, ctx_hi=14000, block_size=bs,
                    q_blocks=q_blocks)
     rng = np.random.default_rng(seed)
