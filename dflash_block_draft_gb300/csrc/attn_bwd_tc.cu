@@ -758,6 +758,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool bwd_tc_supported(int dn, int dr, int dv) { return dn == kDn && dr == kDr && dv == kDv; }
 
+namespace {
+// A second stream per host thread and device, with the fork and join events.
+struct Fork {
+  bool ok;
+  cudaStream_t aux;
+  cudaEvent_t join;
+};
+Fork fork_stream(cudaStream_t stream) {
+  struct Aux {
+    int dev = -1;
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+  };
+  constexpr int kMaxDev = 64;
+  static thread_local Aux aux[kMaxDev];
+  Fork f{false, nullptr, nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return f;
+  Aux& x = aux[dev];
+  if (x.dev != dev) {
+    if (cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess)
+      return f;
+    x.dev = dev;
+  }
+  if (cudaEventRecord(x.fork, stream) != cudaSuccess || cudaStreamWaitEvent(x.s, x.fork, 0) != cudaSuccess)
+    return f;
+  f.ok = true;
+  f.aux = x.s;
+  f.join = x.join;
+  return f;
+}
+cudaError_t join_stream(const Fork& f, cudaStream_t stream) {
+  cudaError_t e = cudaEventRecord(f.join, f.aux);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, f.join, 0);
+  return e;
+}
+}  // namespace
+
 cudaError_t launch_attn_bwd_tc(const AttnParams& p, const float* lse, const void* dout, void* dq, void* dkn,
                                void* dv, const float* D, float* dkr_acc, const int* tile_amax64,
                                const int* tile_amin64, cudaStream_t stream) {
@@ -797,10 +837,15 @@ cudaError_t launch_attn_bwd_tc(const AttnParams& p, const float* lse, const void
     const long long ng = std::max(1LL, ((long long)zh * ntiles + 3LL * nsm / 2) / (3LL * nsm));  // groups, rounded
     return (int)((zh + ng - 1) / ng);
   };
+  // dq and dk/dv are independent: dq runs on a second stream (forked from and
+  // joined back into the caller's), so that each grid's last, partial wave of
+  // CTAs is filled by the other's.
+  const Fork fk = fork_stream(stream);
+  if (!fk.ok) return cudaErrorUnknown;
   if (p.Q > 0) {
     const int nq = (p.Q + 127) / 128;
     a.group = dense ? 0 : group_for(nq);
-    kdq<<<(unsigned)((long long)zh * nq), kThreads, kSmemBytes, stream>>>(a, q128, do128, kn64, kr64, v64);
+    kdq<<<(unsigned)((long long)zh * nq), kThreads, kSmemBytes, fk.aux>>>(a, q128, do128, kn64, kr64, v64);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -808,7 +853,8 @@ cudaError_t launch_attn_bwd_tc(const AttnParams& p, const float* lse, const void
   a.group = dense ? 0 : group_for(nk);
   kkv<<<(unsigned)((long long)zh * nk), kThreads, kSmemBytes, stream>>>(a, q64, do64, kn128, kr128, v128);
   count_launch();
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return join_stream(fk, stream);
 }
 
 }  // namespace dflash

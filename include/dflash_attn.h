@@ -263,8 +263,12 @@ enum {
  *     bytes, 256-byte aligned, device memory; needs no initialisation.
  * Limits: d_nope + d_rope <= DFLASH_BWD_MAX_DQK and d_v <= DFLASH_BWD_MAX_DV
  * (else DFLASH_ERR_UNSUPPORTED).  Device pointers, 16-byte aligned; the call
- * is asynchronous on `stream` and allocates nothing.  Errors as for the
- * forward entry points.
+ * is asynchronous on `stream` and allocates no device memory.  On the
+ * tensor-core path (bf16, head dims 128/64/128) the dq kernel runs on a second
+ * stream that the library creates once per host thread and device; it is
+ * forked from `stream` (an event) and joined back into it before the call
+ * returns, so work queued on `stream` afterwards sees every gradient.  Errors
+ * as for the forward entry points.
  */
 #define DFLASH_BWD_MAX_DQK 256
 #define DFLASH_BWD_MAX_DV 128
