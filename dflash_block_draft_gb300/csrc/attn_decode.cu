@@ -529,9 +529,15 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(AttnParams p,
 }
 
 // Merge the split partials of every (query row, head): one CTA of kDv threads.
-__global__ void __launch_bounds__(kDv) decode_combine_kernel(AttnParams p, const int* prefix, const float* part_o,
-                                                            const float* part_lse, int max_slots) {
-  const int row = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+// One warp per (row, head); a lane owns 4 consecutive dv values (16-byte loads).
+constexpr int kCombineWarps = 8;
+__global__ void __launch_bounds__(32 * kCombineWarps) decode_combine_kernel(AttnParams p, const int* prefix,
+                                                                             const float* part_o,
+                                                                             const float* part_lse, int max_slots) {
+  const long long wid = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= (long long)p.total_q * p.H) return;
+  const int row = (int)(wid / p.H), h = (int)(wid % p.H);
   int lo = 0, hi = p.R - 1;  // request owning this row
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -544,18 +550,27 @@ __global__ void __launch_bounds__(kDv) decode_combine_kernel(AttnParams p, const
   if (u1 <= u0 || q < 0 || q >= kQN || q >= p.q_off[r + 1] - p.q_off[r]) return;  // skipped request
   float M = -INFINITY;
   for (int u = u0; u < u1; ++u) M = fmaxf(M, part_lse[((long long)u * p.H + h) * kQN + q]);
-  float acc = 0.f, wsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
   if (M != -INFINITY) {
     for (int u = u0; u < u1; ++u) {
       const float ls = part_lse[((long long)u * p.H + h) * kQN + q];
       const float w = ls == -INFINITY ? 0.f : __expf(ls - M);
       wsum += w;
-      acc = fmaf(w, part_o[(((long long)u * p.H + h) * kQN + q) * kDv + d], acc);
+      const float4 o = reinterpret_cast<const float4*>(part_o + (((long long)u * p.H + h) * kQN + q) * kDv)[lane];
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
     }
   }
-  const float o = wsum > 0.f ? acc / wsum : 0.f;
-  static_cast<__nv_bfloat16*>(p.out)[((long long)row * p.H + h) * kDv + d] = __float2bfloat16_rn(o);
-  if (p.lse && d == 0) p.lse[(long long)h * p.total_q + row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat162 v01 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv), v23 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&v01);
+  pk.y = *reinterpret_cast<uint32_t*>(&v23);
+  reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + ((long long)row * p.H + h) * kDv)[lane] = pk;
+  if (p.lse && lane == 0) p.lse[(long long)h * p.total_q + row] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
 }  // namespace
@@ -599,7 +614,8 @@ cudaError_t launch_attn_decode(const AttnParams& p, void* ws, cudaStream_t strea
   const int grid = (int)((size_t)nsm < units ? (size_t)nsm : units);
   attn_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, mq, mkn, mkr, mv);
   count_launch();
-  decode_combine_kernel<<<dim3(p.total_q, p.H), kDv, 0, stream>>>(p, a.prefix, a.part_o, a.part_lse, a.max_slots);
+  decode_combine_kernel<<<(unsigned)(((long long)p.total_q * p.H + kCombineWarps - 1) / kCombineWarps),
+                          32 * kCombineWarps, 0, stream>>>(p, a.prefix, a.part_o, a.part_lse, a.max_slots);
   count_launch();
   return cudaGetLastError();
 }
