@@ -1,8 +1,8 @@
 """The bounded-wait failure path of the forward kernels, made to happen on
 purpose without faulting the GPU.
 
-Every mbarrier wait of the tensor-core and split-context decode kernels gives
-up after a budget, records DFLASH_ERR_TIMEOUT in the device error word, and
+Every mbarrier wait of the tensor-core, split-context decode and latent
+attention kernels gives up after a budget, records DFLASH_ERR_TIMEOUT in the device error word, and
 the CTA winds down (its TMA loads land, its MMAs complete, TMEM is freed).
 Here one CTA's producer leaves its first work item's key tiles unloaded (a
 phase nothing will complete) under a 20 ms budget; the test checks the error
@@ -84,6 +84,29 @@ def test_decode_wait_runs_out_then_context_is_usable(dfl):
     assert dfl.dflash_last_device_error() == 0
     want, _ = oracle.ragged(d["q"], d["k_nope"], d["k_rope"], d["v"], d["q_offsets"], d["kv_offsets"],
                             d["anchors"], 16)
+    assert max_abs_err(to_numpy_f64(out2), want) <= TOL["bf16"]
+
+
+def test_latent_wait_runs_out_then_context_is_usable(dfl, monkeypatch):
+    """The absorbed latent attention kernel (bf16 decode shape): one CTA's
+    producer leaves its first unit's key tiles unloaded."""
+    monkeypatch.delenv("DFLASH_LATENT_EXPAND", raising=False)
+    d = synth.make("decode_latent_bf16", seed=63, R=4, H=8, ctx_lo=1500, ctx_hi=5000)
+    t = {k: to_torch(d[k], "bf16") for k in ("q", "c_kv", "k_rope", "w_kv_b")}
+    qo, ko, an = (torch.from_numpy(d[k]).cuda() for k in ("q_offsets", "kv_offsets", "anchors"))
+    out = torch.empty((d["total_q"], 8, 128), dtype=torch.bfloat16, device="cuda")
+
+    def call(o):
+        dfl.dflash_attn_latent_ragged(t["q"], t["c_kv"], t["k_rope"], t["w_kv_b"], qo, ko, an, d["block_size"], 16,
+                                      out=o)
+
+    st, secs = _stalled(dfl, lambda: call(out))
+    assert st == DFLASH_ERR_TIMEOUT and secs < 1.5
+    out2 = torch.full_like(out, float("nan"))
+    call(out2)
+    assert dfl.dflash_last_device_error() == 0
+    want, _ = oracle.latent_ragged(d["q"], d["c_kv"], d["k_rope"], d["w_kv_b"], d["q_offsets"], d["kv_offsets"],
+                                   d["anchors"], d["block_size"])
     assert max_abs_err(to_numpy_f64(out2), want) <= TOL["bf16"]
 
 
