@@ -157,13 +157,14 @@ struct Smem {
   uint32_t* tmem_slot;
 };
 
-__device__ __forceinline__ Smem setup_smem(uint8_t* raw, unsigned* err) {
+__device__ __forceinline__ Smem setup_smem(uint8_t* raw, const AttnParams& p) {
   Smem s;
   s.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   s.sbase = ptx::smem_u32(s.base);
   s.ctl.bar0 = s.sbase + kOffBar;
   s.ctl.abort = reinterpret_cast<volatile int*>(s.base + kOffAbort);
-  s.ctl.err = err;
+  s.ctl.err = p.err;
+  s.ctl.budget = p.wait_ns;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.base + kOffSlot);
   return s;
 }
@@ -217,6 +218,16 @@ __device__ __forceinline__ void drain(const Smem& s) {
   }
 }
 
+// The TMA thread's last act (also after a timeout): every load it issued -- the
+// fixed tiles and at most the last kStages stages -- lands before the CTA exits,
+// since a copy still in flight would write into shared memory the CTA no longer
+// owns.
+__device__ __forceinline__ void loads_landed(const Smem& s, uint32_t stages_issued) {
+  s.ctl.wait_landed(BAR_FIXED, 0);
+  for (uint32_t i = stages_issued > kStages ? stages_issued - kStages : 0u; i < stages_issued; ++i)
+    s.ctl.wait_landed(BAR_FULL + i % kStages, (i / kStages) & 1u);
+}
+
 __device__ __forceinline__ void teardown(const Smem& s, uint32_t tmem) {
   ptx::tc_fence_before();
   __syncthreads();
@@ -237,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmKr, const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];
   const AttnParams& p = a.p;
-  const Smem s = setup_smem(smem_raw, p.err);
+  const Smem s = setup_smem(smem_raw, p);
   const Ctl& ctl = s.ctl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // The last query tiles first: under sorted anchors they see the most context.
@@ -267,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int pn = 0; pn < 3; ++pn) ptx::tma_load_3d(sQ + pn * kP128, &tmQ, ctl.bar(BAR_FIXED), 64 * pn, h, qrow);
       for (int pn = 0; pn < 2; ++pn) ptx::tma_load_3d(sDO + pn * kP128, &tmDO, ctl.bar(BAR_FIXED), 64 * pn, h, qrow);
       uint32_t j = 0;
-      for (int kt = 0; kt < nkt; ++kt) {
+      // (timeout test: the stalled CTA's key tiles never arrive)
+      for (int kt = 0; kt < nkt && (int)blockIdx.x != p.stall_cta; ++kt) {
         if (!needed(kt)) continue;
         const uint32_t st = j % kStages;
         if (!ctl.wait(BAR_EMPTY + st, ((j / kStages) & 1u) ^ 1u)) break;
@@ -281,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_3d(dst + 4 * kP64, &tmV, fb, 64, h, krow);
         ++j;
       }
+      loads_landed(s, j);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -463,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmKr, const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];
   const AttnParams& p = a.p;
-  const Smem s = setup_smem(smem_raw, p.err);
+  const Smem s = setup_smem(smem_raw, p);
   const Ctl& ctl = s.ctl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // The first key tiles first: under sorted anchors the most query rows see them.
@@ -492,7 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tma_load_3d(sV, &tmV, ctl.bar(BAR_FIXED), 0, h, krow);
       ptx::tma_load_3d(sV + kP128, &tmV, ctl.bar(BAR_FIXED), 64, h, krow);
       uint32_t j = 0;
-      for (int t = 0; t < nqt; ++t) {
+      // (timeout test: the stalled CTA's query tiles never arrive)
+      for (int t = 0; t < nqt && (int)blockIdx.x != p.stall_cta; ++t) {
         if (!needed(t)) continue;
         const uint32_t st = j % kStages;
         if (!ctl.wait(BAR_EMPTY + st, ((j / kStages) & 1u) ^ 1u)) break;
@@ -503,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int pn = 0; pn < 2; ++pn) ptx::tma_load_3d(dst + (3 + pn) * kP64, &tmDO, fb, 64 * pn, h, qrow);
         ++j;
       }
+      loads_landed(s, j);
     }
   } else if (warp == 1) {
     if (lane == 0) {

@@ -335,17 +335,18 @@ DFLASH_API dflash_status_t dflash_build_mask(int B, int S, int Q, const int32_t*
 
 /*
  * Test export: fault injection for the bounded-wait path.  Every mbarrier wait
- * of the forward kernels (tensor-core and split-context decode) gives up after
- * a budget -- 2 s unless set here -- records DFLASH_ERR_TIMEOUT in the device
- * error word, and the CTA winds down: its issued TMA loads land, its issued
- * MMAs complete, its TMEM is freed, and it returns; the context stays usable.
- * This call sets, process-wide and for every later forward call until it is
- * called again:
+ * of the tensor-core kernels (forward, split-context decode, latent decode and
+ * backward) gives up after a budget -- 2 s unless set here -- records
+ * DFLASH_ERR_TIMEOUT in the device error word, and the CTA winds down: its
+ * issued TMA loads land, its issued MMAs complete, its TMEM is freed, and it
+ * returns; the context stays usable.  This call sets, process-wide and for
+ * every later call until it is called again:
  *   wait_budget_ns  budget of one wait (0 restores the 2 s default);
- *   stall_cta       the CTA whose TMA producer leaves its first work item's
- *                   key tiles unloaded, so that the waits on them run out
- *                   (-1: none).  Other CTAs compute normally; the stalled
- *                   CTA's output rows are left unwritten.
+ *   stall_cta       the CTA (of each of those kernels) whose TMA producer
+ *                   leaves its first work item's key tiles (the backward's
+ *                   dk/dv kernel: query tiles) unloaded, so that the waits on
+ *                   them run out (-1: none).  Other CTAs compute normally; the
+ *                   stalled CTA's results are left unwritten or incomplete.
  * Not for production use; not synchronised with calls in flight.
  */
 DFLASH_API void dflash_test_inject_stall(unsigned long long wait_budget_ns, int stall_cta);

@@ -1,8 +1,8 @@
 """The bounded-wait failure path of the forward kernels, made to happen on
 purpose without faulting the GPU.
 
-Every mbarrier wait of the tensor-core, split-context decode and latent
-attention kernels gives up after a budget, records DFLASH_ERR_TIMEOUT in the device error word, and
+Every mbarrier wait of the tensor-core (forward and backward), split-context
+decode and latent attention kernels gives up after a budget, records DFLASH_ERR_TIMEOUT in the device error word, and
 the CTA winds down (its TMA loads land, its MMAs complete, TMEM is freed).
 Here one CTA's producer leaves its first work item's key tiles unloaded (a
 phase nothing will complete) under a 20 ms budget; the test checks the error
@@ -108,6 +108,34 @@ def test_latent_wait_runs_out_then_context_is_usable(dfl, monkeypatch):
     want, _ = oracle.latent_ragged(d["q"], d["c_kv"], d["k_rope"], d["w_kv_b"], d["q_offsets"], d["kv_offsets"],
                                    d["anchors"], d["block_size"])
     assert max_abs_err(to_numpy_f64(out2), want) <= TOL["bf16"]
+
+
+def test_backward_wait_runs_out_then_context_is_usable(dfl, monkeypatch):
+    """The tensor-core backward kernels (dq and dk/dv): CTA 0 of each grid gets
+    no key (dq) or query (dk/dv) tiles."""
+    monkeypatch.delenv("DFLASH_FORCE_SIMT", raising=False)
+    d = synth.make("tiny_fp32", seed=64, dtype="bf16", B=1, H=2, S=600, nb=20, block_size=16, d_nope=128,
+                   d_rope=64, d_v=128, anchor_lo=0, anchor_hi=601)
+    d["dout"] = synth.make_dout(d)
+    t = {k: to_torch(d[k], "bf16") for k in ("q", "k_nope", "k_rope", "v", "dout")}
+    an = torch.from_numpy(d["anchors"]).cuda()
+    out = torch.empty((1, d["Q"], 2, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 2, d["Q"]), dtype=torch.float32, device="cuda")
+    dfl.dflash_attn_anchored(t["q"], t["k_nope"], t["k_rope"], t["v"], an, 16, out=out, lse=lse)
+    assert dfl.dflash_last_device_error() == 0
+
+    def call():
+        return dfl.dflash_attn_anchored_backward(t["q"], t["k_nope"], t["k_rope"], t["v"], an, 16, out, lse,
+                                                 t["dout"])
+
+    st, secs = _stalled(dfl, call)
+    assert st == DFLASH_ERR_TIMEOUT and secs < 1.5
+    got = [to_numpy_f64(x) for x in call()]
+    assert dfl.dflash_last_device_error() == 0
+    want = oracle.backward(d["q"], d["k_nope"], d["k_rope"], d["v"], d["dout"], anchors=d["anchors"],
+                           block_size=16)
+    for name, g, w in zip(("dq", "dk_nope", "dk_rope", "dv"), got, want):
+        np.testing.assert_allclose(g, w, atol=2e-2, rtol=2.0 ** -7, err_msg=name)
 
 
 def test_no_stall_leaves_the_default_budget(dfl):
