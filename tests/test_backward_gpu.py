@@ -173,6 +173,24 @@ def test_backward_prefill_workload_every_element(dfl, kernel):
     _compare(_gpu(dfl, d, "bf16"), want, "bf16")
 
 
+def test_backward_training_workload_sampled_heads(dfl):
+    """The bf16 training workload at full size (B=4 H=32 S=8192 nb=512
+    block_size=16), in the launch configuration the benchmark times: every
+    element of dq, dk_nope and dv of two (batch row, head) pairs, the first and
+    the last, against the oracle evaluated on those pairs alone (dk_rope sums
+    over all heads, so it is left to the every-element tests)."""
+    d = synth.make("training_bf16")
+    d["dout"] = synth.make_dout(d)
+    got = _gpu(dfl, d, "bf16")
+    B, H = d["B"], d["H"]
+    pairs = [(0, 0), (B - 1, H - 1)]
+    want = _oracle(d, pairs=[b * H + h for b, h in pairs])
+    for b, h in pairs:
+        for name, i in (("dq", 0), ("dk_nope", 1), ("dv", 3)):
+            np.testing.assert_allclose(got[i][b, :, h], want[i][b, :, h], atol=ATOL["bf16"], rtol=RTOL["bf16"],
+                                       err_msg=f"{name} (b={b}, h={h})")
+
+
 @pytest.mark.parametrize("shape", [
     # B, H, S, nb, bs: query and key tails that are not multiples of 64 or 128
     (2, 2, 77, 9, 7),
