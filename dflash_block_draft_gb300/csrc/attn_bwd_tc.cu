@@ -775,6 +775,9 @@ bool bwd_tc_supported(int dn, int dr, int dv) { return dn == kDn && dr == kDr &&
 
 namespace {
 // A second stream per host thread and device, with the fork and join events.
+// They are created on first use and kept for the life of the process (a
+// cudaDeviceReset by the caller invalidates them: later backward calls on that
+// thread then fail with DFLASH_ERR_CUDA).
 struct Fork {
   bool ok;
   cudaStream_t aux;
