@@ -37,6 +37,7 @@ EXPORTS = ("dflash_attn_dense", "dflash_attn_anchored", "dflash_attn_ragged", "d
            "dflash_build_schedule_host", "dflash_scan_mask", "dflash_status_string", "dflash_last_device_error",
            "dflash_kernel_launches", "dflash_attn_dense_noalloc", "dflash_build_mask",
            "dflash_attn_anchored_backward", "dflash_attn_dense_backward", "dflash_test_inject_stall",
+           "dflash_test_limit_tile_flags",
            "dflash_attn_latent_ragged", "dflash_attn_latent_workspace_size")
 
 
@@ -94,6 +95,8 @@ def load_library(path: str | None = None):
         lib.dflash_attn_latent_workspace_size.restype = S
         lib.dflash_test_inject_stall.argtypes = [ctypes.c_ulonglong, I]
         lib.dflash_test_inject_stall.restype = None
+        lib.dflash_test_limit_tile_flags.argtypes = [I]
+        lib.dflash_test_limit_tile_flags.restype = None
         lib.dflash_kernel_launches.argtypes = []
         lib.dflash_kernel_launches.restype = ctypes.c_uint64
         for name in ("dflash_attn_dense", "dflash_attn_anchored", "dflash_attn_ragged",
@@ -441,3 +444,9 @@ def dflash_test_inject_stall(wait_budget_ns: int = 0, stall_cta: int = -1) -> No
     whose producer leaves its first work item's key tiles unloaded (-1 = none),
     for every later forward call in this process."""
     load_library().dflash_test_inject_stall(int(wait_budget_ns), int(stall_cta))
+
+
+def dflash_test_limit_tile_flags(n: int = 0) -> None:
+    """Test export: cap the backward kernels' shared-memory table of tile flags
+    at n entries (0 = the full table), for every later call in this process."""
+    load_library().dflash_test_limit_tile_flags(int(n))

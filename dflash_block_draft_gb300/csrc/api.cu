@@ -3,6 +3,7 @@
 // Every entry point validates on the host before it launches anything, then
 // enqueues its kernels on the caller's stream and returns without
 // synchronising.  No device memory is allocated here.
+#include <limits.h>
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -22,6 +23,8 @@ std::atomic<uint64_t> g_launches{0};
 // Test fault injection (dflash_test_inject_stall): wait budget and stalled CTA.
 std::atomic<unsigned long long> g_wait_ns{0};
 std::atomic<int> g_stall_cta{-1};
+// Test hook (dflash_test_limit_tile_flags): backward tile flags kept in shared memory.
+std::atomic<int> g_flag_tiles{0};
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 }
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -172,6 +175,8 @@ AttnParams base_params(int H, int dn, int dr, int dv, float scale, const void* q
   const unsigned long long w = g_wait_ns.load(std::memory_order_relaxed);
   p.wait_ns = w ? w : kDefaultWaitNs;
   p.stall_cta = g_stall_cta.load(std::memory_order_relaxed);
+  const int nf = g_flag_tiles.load(std::memory_order_relaxed);
+  p.flag_tiles = nf > 0 ? nf : INT_MAX;
   return p;
 }
 
@@ -576,6 +581,8 @@ void dflash_test_inject_stall(unsigned long long wait_budget_ns, int stall_cta) 
   g_wait_ns.store(wait_budget_ns, std::memory_order_relaxed);
   g_stall_cta.store(stall_cta < 0 ? -1 : stall_cta, std::memory_order_relaxed);
 }
+
+void dflash_test_limit_tile_flags(int n) { g_flag_tiles.store(n > 0 ? n : 0, std::memory_order_relaxed); }
 
 dflash_status_t dflash_last_device_error(dflash_stream_t stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DFLASH_ERR_CUDA;

@@ -86,7 +86,9 @@ enum {
 };
 constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;
 constexpr uint32_t kOffAbort = kOffSlot + 4;
-constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;
+constexpr uint32_t kOffFlags = (kOffAbort + 4 + 15) & ~15u;  // tile flags: dq per key tile, dkdv per query tile
+constexpr int kFlagTiles = 16384;                              // entries of the flag table
+constexpr uint32_t kSmemBytes = kOffFlags + kFlagTiles + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kIdScore = ptx::idesc_bf16_f32(128, 64, 0, 0);  // both K-major
@@ -264,9 +266,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     amax = a.tile_amax[ti];
     if (r0 + 64 < Q) amax = max(amax, a.tile_amax[ti + 1]);
   }
-  auto needed = [&](int kt) { return pair_needed(a, b, r0, r1, kt * 64, min(kt * 64 + 64, K), amax); };
+  // Per 64-key tile: bit 0 = some (row, key) pair of this query tile and it is
+  // visible, bit 1 (dense) = its mask tile is all 0.  Worked out once per CTA
+  // into a shared-memory table (dense: the class loads of all tiles in flight
+  // together); tiles past the table are worked out when they come up.
+  auto tile_flags = [&](int kt) -> uint32_t {
+    const uint32_t need = pair_needed(a, b, r0, r1, kt * 64, min(kt * 64 + 64, K), amax) ? 1u : 0u;
+    if (!DENSE) return need;
+    return need | (p.classes[((long long)b * p.nqt + t) * p.nkt + (kt * 64) / kTileN] == DFLASH_TILE_FULL ? 2u : 0u);
+  };
+  uint8_t* tfl = s.base + kOffFlags;
+  const int nflag = min(min(nkt, kFlagTiles), p.flag_tiles);
+  for (int kt = threadIdx.x; kt < nflag; kt += kThreads) tfl[kt] = (uint8_t)tile_flags(kt);
+  auto flags = [&](int kt) -> uint32_t { return kt < nflag ? tfl[kt] : tile_flags(kt); };
+  auto needed = [&](int kt) { return (flags(kt) & 1u) != 0u; };
 
-  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV);
+  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV);  // its barrier publishes the flags
   const uint32_t tmem = *s.tmem_slot;
   const uint32_t sQ = s.sbase + kOffFixed, sDO = sQ + 3 * kP128, sSt = s.sbase + kOffStage;
 
@@ -377,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row_ok) {
         if (DENSE) {
           vis = (uint32_t)range_bits(0, K - k0);
-          full_tile = p.classes[((long long)b * p.nqt + t) * p.nkt + (kt * 64) / kTileN] == DFLASH_TILE_FULL;
+          full_tile = (flags(kt) & 2u) != 0u;
         } else {
           vis = (uint32_t)((range_bits(0, ctx - k0) | range_bits(nlo - k0, nhi - k0)) & range_bits(0, K - k0));
         }
@@ -485,12 +500,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = p.S, Q = p.Q, K = S + Q;
   const int k0 = kt * 128, k1 = min(k0 + 128, K);
   const int nqt = a.nqt64;
-  auto needed = [&](int t) {
-    const int amax = DENSE ? 0 : a.tile_amax[(long long)b * nqt + t];
-    return pair_needed(a, b, t * 64, min(t * 64 + 64, Q), k0, k1, amax);
+  // Per 64-row query tile: bit 0 = some (row, key) pair of it and this key tile
+  // is visible, bit 1 = every pair is.  Worked out once per CTA, with the loads
+  // of all tiles in flight together, into a shared-memory table; tiles past the
+  // table are worked out when they come up.
+  auto tile_flags = [&](int t) -> uint32_t {
+    const long long ti = (long long)b * nqt + t;
+    const bool whole = t * 64 + 64 <= Q;
+    if (DENSE) {
+      const uint8_t c = p.classes[((long long)b * p.nqt + (t * 64) / kTileM) * p.nkt + kt];
+      return (c != DFLASH_TILE_SKIP ? 1u : 0u) | (whole && k1 <= K && c == DFLASH_TILE_FULL ? 2u : 0u);
+    }
+    const int amax = a.tile_amax[ti], amin = a.tile_amin[ti];
+    return (pair_needed(a, b, t * 64, min(t * 64 + 64, Q), k0, k1, amax) ? 1u : 0u) |
+           (whole && k1 <= S && k1 <= amin ? 2u : 0u);
   };
+  uint8_t* tfl = s.base + kOffFlags;
+  const int nflag = min(min(nqt, kFlagTiles), p.flag_tiles);
+  for (int t = threadIdx.x; t < nflag; t += kThreads) tfl[t] = (uint8_t)tile_flags(t);
+  auto flags = [&](int t) -> uint32_t { return t < nflag ? tfl[t] : tile_flags(t); };
+  auto needed = [&](int t) { return (flags(t) & 1u) != 0u; };
 
-  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV);
+  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV);  // its barrier publishes the flags
   const uint32_t tmem = *s.tmem_slot;
   const uint32_t sK = s.sbase + kOffFixed, sV = sK + 3 * kP128, sSt = s.sbase + kOffStage;
 
@@ -642,12 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t_after = next_needed(t);
       const int r0 = t * 64 + 32 * (int)half;  // this warp's first query row
       // every (row, key) pair of the 64 x 128 tile visible: no per-pair mask
-      bool full_tile;
-      if (DENSE)
-        full_tile = t * 64 + 64 <= Q && k1 <= K &&
-                    p.classes[((long long)b * p.nqt + (t * 64) / kTileM) * p.nkt + kt] == DFLASH_TILE_FULL;
-      else
-        full_tile = t * 64 + 64 <= Q && k1 <= S && k1 <= a.tile_amin[(long long)b * nqt + t];
+      const bool full_tile = (flags(t) & 2u) != 0u;
       __syncwarp();
       cl[lane] = nxt.l;
       cD[lane] = nxt.d;

@@ -48,6 +48,9 @@ struct AttnParams {
   // item's key tiles unloaded so that its consumers' waits run out.
   unsigned long long wait_ns;
   int stall_cta;
+  // Backward: how many tile flags a CTA may keep in shared memory (the kernels
+  // cap it at their table's size; tests of the path past the table lower it).
+  int flag_tiles;
 };
 
 // One segment (batch row or request), resolved on the device.

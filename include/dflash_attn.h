@@ -351,6 +351,17 @@ DFLASH_API dflash_status_t dflash_build_mask(int B, int S, int Q, const int32_t*
  */
 DFLASH_API void dflash_test_inject_stall(unsigned long long wait_budget_ns, int stall_cta);
 
+/*
+ * Test export: the backward kernels work out, once per CTA, which tiles of the
+ * axis they loop over (dq: key tiles; dk/dv: query tiles) they need, and keep
+ * these flags in a shared-memory table of 16384 entries; tiles past the table
+ * are worked out when they come up.  This call caps the table at n entries
+ * (n <= 0 restores the full table), process-wide for every later call, so that
+ * tests reach the path past the table at small sizes.  Results do not depend
+ * on n.  Not for production use; not synchronised with calls in flight.
+ */
+DFLASH_API void dflash_test_limit_tile_flags(int n);
+
 /* Human-readable name of a status code (static storage). */
 DFLASH_API const char* dflash_status_string(dflash_status_t status);
 

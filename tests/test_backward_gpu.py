@@ -246,3 +246,26 @@ def test_bf16_dense_backward_row_with_no_visible_key(dfl, kernel):
     got = _gpu(dfl, d, "bf16", mask=bits)
     _compare(got, _oracle(d, mask=widened), "bf16")
     assert np.all(got[0][0, 37] == 0.0)
+
+
+@pytest.mark.parametrize("masked", [False, True], ids=["anchored", "dense"])
+@pytest.mark.parametrize("limit", [1, 3])
+def test_tc_backward_tiles_past_the_flag_table(dfl, limit, masked, monkeypatch):
+    """The tensor-core backward works out once per CTA which tiles it needs (and
+    which need no per-pair mask) into a shared-memory table, and the tiles past
+    the table when they come up.  With the table capped at `limit` entries most
+    tiles (of 10 key tiles for dq, 5 query tiles for dk/dv) take that path: the
+    gradients still match the oracle, and dq, dk_nope and dv (no atomics) are
+    bit-identical to those of the full table."""
+    monkeypatch.delenv("DFLASH_FORCE_SIMT", raising=False)
+    d = _case("bf16", 1, 2, 300, 20, 16, 128, 64, 128, seed=41)
+    dev_mask, ora_mask = _mask(d, "bf16") if masked else (None, None)
+    full = _gpu(dfl, d, "bf16", mask=dev_mask)
+    try:
+        dfl.dflash_test_limit_tile_flags(limit)
+        got = _gpu(dfl, d, "bf16", mask=dev_mask)
+    finally:
+        dfl.dflash_test_limit_tile_flags(0)
+    _compare(got, _oracle(d, mask=ora_mask), "bf16")
+    for i in (0, 1, 3):
+        np.testing.assert_array_equal(got[i], full[i])
