@@ -86,9 +86,11 @@ enum {
 };
 constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;
 constexpr uint32_t kOffAbort = kOffSlot + 4;
-constexpr uint32_t kOffFlags = (kOffAbort + 4 + 15) & ~15u;  // tile flags: dq per key tile, dkdv per query tile
-constexpr int kFlagTiles = 16384;                              // entries of the flag table
-constexpr uint32_t kSmemBytes = kOffFlags + kFlagTiles + 1024;
+// Tile table (dq: key tiles, dkdv: query tiles): two bit arrays, need and full.
+constexpr int kFlagTiles = 16384;  // tiles the table covers
+constexpr uint32_t kFlagWords = kFlagTiles / 32;
+constexpr uint32_t kOffFlags = (kOffAbort + 4 + 15) & ~15u;
+constexpr uint32_t kSmemBytes = kOffFlags + 2 * kFlagWords * 4 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kIdScore = ptx::idesc_bf16_f32(128, 64, 0, 0);  // both K-major
@@ -150,6 +152,48 @@ __device__ __forceinline__ bool pair_needed(const BwdTcArgs& a, int b, int r0, i
   const int u0 = p.S + (r0 / p.bs) * p.bs;
   const int u1 = p.S + min(((r1 - 1) / p.bs + 1) * p.bs, p.Q);
   return k0 < u1 && k1 > u0;
+}
+
+// The tile table of a CTA: bit i of need says that some (row, key) pair of
+// tile i is visible, bit i of full that every pair is.  The table covers the
+// first n tiles of the axis; eval(i) works out tile i's flags (bit 0 need, bit
+// 1 full) for the tiles past it.  Built once per CTA by all its warps (32 tiles
+// per ballot), so that the roles find the next tile they need with a bit scan
+// instead of a load per tile.
+template <typename Eval>
+struct TileTable {
+  uint32_t* need;
+  uint32_t* full;
+  int n, total;
+  Eval eval;
+  __device__ void build() const {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int base = 32 * warp; base < n; base += blockDim.x) {
+      const int i = base + lane;
+      const uint32_t f = i < n ? eval(i) : 0u;
+      const uint32_t nb = __ballot_sync(0xffffffffu, f & 1u), fb = __ballot_sync(0xffffffffu, (f & 2u) != 0u);
+      if (lane == 0) {
+        need[base >> 5] = nb;
+        full[base >> 5] = fb;
+      }
+    }
+  }
+  // First needed tile after t (total when none is left).
+  __device__ int next(int t) const {
+    for (int i = t + 1; i < n; i = (i | 31) + 1) {
+      const uint32_t w = need[i >> 5] >> (i & 31);
+      if (w) return i + __ffs(w) - 1;
+    }
+    for (int i = max(t + 1, n); i < total; ++i)
+      if (eval(i) & 1u) return i;
+    return total;
+  }
+  __device__ bool is_full(int i) const { return i < n ? (full[i >> 5] >> (i & 31)) & 1u : (eval(i) & 2u) != 0u; }
+};
+template <typename Eval>
+__device__ __forceinline__ TileTable<Eval> tile_table(uint8_t* base, int n, int total, int cap, Eval eval) {
+  uint32_t* need = reinterpret_cast<uint32_t*>(base + kOffFlags);
+  return TileTable<Eval>{need, need + kFlagWords, min(min(n, kFlagTiles), cap), total, eval};
 }
 
 struct Smem {
@@ -267,19 +311,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (r0 + 64 < Q) amax = max(amax, a.tile_amax[ti + 1]);
   }
   // Per 64-key tile: bit 0 = some (row, key) pair of this query tile and it is
-  // visible, bit 1 (dense) = its mask tile is all 0.  Worked out once per CTA
-  // into a shared-memory table (dense: the class loads of all tiles in flight
-  // together); tiles past the table are worked out when they come up.
+  // visible, bit 1 (dense) = its mask tile is all 0.
   auto tile_flags = [&](int kt) -> uint32_t {
     const uint32_t need = pair_needed(a, b, r0, r1, kt * 64, min(kt * 64 + 64, K), amax) ? 1u : 0u;
     if (!DENSE) return need;
     return need | (p.classes[((long long)b * p.nqt + t) * p.nkt + (kt * 64) / kTileN] == DFLASH_TILE_FULL ? 2u : 0u);
   };
-  uint8_t* tfl = s.base + kOffFlags;
-  const int nflag = min(min(nkt, kFlagTiles), p.flag_tiles);
-  for (int kt = threadIdx.x; kt < nflag; kt += kThreads) tfl[kt] = (uint8_t)tile_flags(kt);
-  auto flags = [&](int kt) -> uint32_t { return kt < nflag ? tfl[kt] : tile_flags(kt); };
-  auto needed = [&](int kt) { return (flags(kt) & 1u) != 0u; };
+  const auto tiles = tile_table(s.base, nkt, nkt, p.flag_tiles, tile_flags);
+  tiles.build();
 
   init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV);  // its barrier publishes the flags
   const uint32_t tmem = *s.tmem_slot;
@@ -294,8 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int pn = 0; pn < 2; ++pn) ptx::tma_load_3d(sDO + pn * kP128, &tmDO, ctl.bar(BAR_FIXED), 64 * pn, h, qrow);
       uint32_t j = 0;
       // (timeout test: the stalled CTA's key tiles never arrive)
-      for (int kt = 0; kt < nkt && (int)blockIdx.x != p.stall_cta; ++kt) {
-        if (!needed(kt)) continue;
+      for (int kt = tiles.next(-1); kt < nkt && (int)blockIdx.x != p.stall_cta; kt = tiles.next(kt)) {
         const uint32_t st = j % kStages;
         if (!ctl.wait(BAR_EMPTY + st, ((j / kStages) & 1u) ^ 1u)) break;
         const uint32_t fb = ctl.bar(BAR_FULL + st), dst = sSt + st * kStageBytes;
@@ -350,8 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       uint32_t j = 0;
-      for (int kt = 0; ok && kt < nkt; ++kt) {
-        if (!needed(kt)) continue;
+      for (int kt = tiles.next(-1); ok && kt < nkt; kt = tiles.next(kt)) {
         ok = issue_scores(j);
         if (ok && j > 0) ok = issue_dq(j - 1);
         ++j;
@@ -384,15 +421,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     uint32_t j = 0;
     bool ok = true;
-    for (int kt = 0; kt < nkt; ++kt) {
-      if (!needed(kt)) continue;
+    for (int kt = tiles.next(-1); kt < nkt; kt = tiles.next(kt)) {
       const int k0 = kt * 64 + 32 * (int)half;  // this warp's first key
       uint32_t vis = 0;
       bool full_tile = false;  // dense: an all-0 mask tile needs no mask reads
       if (row_ok) {
         if (DENSE) {
           vis = (uint32_t)range_bits(0, K - k0);
-          full_tile = (flags(kt) & 2u) != 0u;
+          full_tile = tiles.is_full(kt);
         } else {
           vis = (uint32_t)((range_bits(0, ctx - k0) | range_bits(nlo - k0, nhi - k0)) & range_bits(0, K - k0));
         }
@@ -501,9 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int k0 = kt * 128, k1 = min(k0 + 128, K);
   const int nqt = a.nqt64;
   // Per 64-row query tile: bit 0 = some (row, key) pair of it and this key tile
-  // is visible, bit 1 = every pair is.  Worked out once per CTA, with the loads
-  // of all tiles in flight together, into a shared-memory table; tiles past the
-  // table are worked out when they come up.
+  // is visible, bit 1 = every pair is.
   auto tile_flags = [&](int t) -> uint32_t {
     const long long ti = (long long)b * nqt + t;
     const bool whole = t * 64 + 64 <= Q;
@@ -515,11 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     return (pair_needed(a, b, t * 64, min(t * 64 + 64, Q), k0, k1, amax) ? 1u : 0u) |
            (whole && k1 <= S && k1 <= amin ? 2u : 0u);
   };
-  uint8_t* tfl = s.base + kOffFlags;
-  const int nflag = min(min(nqt, kFlagTiles), p.flag_tiles);
-  for (int t = threadIdx.x; t < nflag; t += kThreads) tfl[t] = (uint8_t)tile_flags(t);
-  auto flags = [&](int t) -> uint32_t { return t < nflag ? tfl[t] : tile_flags(t); };
-  auto needed = [&](int t) { return (flags(t) & 1u) != 0u; };
+  const auto tiles = tile_table(s.base, nqt, nqt, p.flag_tiles, tile_flags);
+  tiles.build();
 
   init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV);  // its barrier publishes the flags
   const uint32_t tmem = *s.tmem_slot;
@@ -537,8 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tma_load_3d(sV + kP128, &tmV, ctl.bar(BAR_FIXED), 64, h, krow);
       uint32_t j = 0;
       // (timeout test: the stalled CTA's query tiles never arrive)
-      for (int t = 0; t < nqt && (int)blockIdx.x != p.stall_cta; ++t) {
-        if (!needed(t)) continue;
+      for (int t = tiles.next(-1); t < nqt && (int)blockIdx.x != p.stall_cta; t = tiles.next(t)) {
         const uint32_t st = j % kStages;
         if (!ctl.wait(BAR_EMPTY + st, ((j / kStages) & 1u) ^ 1u)) break;
         const uint32_t fb = ctl.bar(BAR_FULL + st), dst = sSt + st * kStageBytes;
@@ -597,8 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       uint32_t j = 0;
-      for (int t = 0; ok && t < nqt; ++t) {
-        if (!needed(t)) continue;
+      for (int t = tiles.next(-1); ok && t < nqt; t = tiles.next(t)) {
         if (!wait_stage(j)) {
           ok = false;
           break;
@@ -660,20 +689,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return r;
     };
-    auto next_needed = [&](int t) {
-      for (++t; t < nqt; ++t)
-        if (needed(t)) break;
-      return t;
-    };
     uint32_t j = 0;
     bool ok = true;
-    int t = next_needed(-1);
+    int t = tiles.next(-1);
     RowData nxt = load_row(t);
     for (; t < nqt;) {
-      const int t_after = next_needed(t);
+      const int t_after = tiles.next(t);
       const int r0 = t * 64 + 32 * (int)half;  // this warp's first query row
       // every (row, key) pair of the 64 x 128 tile visible: no per-pair mask
-      const bool full_tile = (flags(t) & 2u) != 0u;
+      const bool full_tile = tiles.is_full(t);
       __syncwarp();
       cl[lane] = nxt.l;
       cD[lane] = nxt.d;
