@@ -721,6 +721,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         dd[4 * v + 2] = d4.z;
         dd[4 * v + 3] = d4.w;
       }
+      // anchored: which of the warp's 32 rows see this thread's key, as a bit mask
+      // worked out before the scores arrive (one short loop, so that the element
+      // loop below carries no per-element selection code)
+      uint32_t vmask = 0xffffffffu;
+      if (!DENSE && !full_tile) {
+        vmask = 0u;
+        if (key_ok) {
+#pragma unroll 4
+          for (int col = 0; col < 32; ++col)
+            vmask |= (r0 + col < Q && (k < cctx[col] || (k >= cnlo[col] && k < cnhi[col])) ? 1u : 0u) << col;
+        }
+      }
       if (!__all_sync(0xffffffffu, ctl.wait(BAR_SP + (j & 1u), (j >> 1) & 1u))) {
         ok = false;
         break;
@@ -746,19 +758,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float x = __uint_as_float(sx[col]);
           float arg;
           bool vis;
-          if (full_tile) {
+          if (!DENSE) {
+            arg = fmaf(x, c2, nl[col]);
+            vis = (vmask >> col) & 1u;
+          } else if (full_tile) {
             arg = fmaf(x, c2, nl[col]);
             vis = true;
           } else {
             const int i = r0 + col;
             float m2 = -INFINITY;
-            if (key_ok && i < Q) {
-              if (DENSE)
-                m2 = mask2(__bfloat162float(
-                    static_cast<const __nv_bfloat16*>(p.mask)[((long long)b * Q + i) * K + k]));
-              else
-                m2 = (k < cctx[col] || (k >= cnlo[col] && k < cnhi[col])) ? 0.f : -INFINITY;
-            }
+            if (key_ok && i < Q)
+              m2 = mask2(__bfloat162float(static_cast<const __nv_bfloat16*>(p.mask)[((long long)b * Q + i) * K + k]));
             vis = m2 != -INFINITY;
             arg = fmaf(x, c2, m2) + nl[col];
           }
