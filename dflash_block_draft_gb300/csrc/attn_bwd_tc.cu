@@ -7,11 +7,15 @@
 // softmax weights recomputed from the forward's lse and D = dout . out:
 //   S = Q K^T,  dP = dO V^T,  dS = P (dP - D)
 //   dQ = scale dS K,   dK = scale dS^T Q,   dV = P^T dO
-// Two kernels, each one CTA per tile, 320 threads: warp 0 issues TMA loads,
-// warp 1 owns TMEM and issues the MMAs, warps 2..9 do the elementwise work and
-// the epilogue.  Those are two warps per TMEM lane quarter (one TMEM lane = one
-// row per thread); the two split each tile's 64 columns in halves, so that two
-// warps per sub-partition hide each other's latency.
+// Two kernels, each one CTA per tile, 352 threads: warp 0 issues TMA loads,
+// warp 1 owns TMEM and issues S (S^T) and the accumulating MMAs, warp 10
+// issues dP (dP^T), warps 2..9 do the elementwise work and the epilogue.  The
+// elementwise warps are two per TMEM lane quarter (one TMEM lane = one row per
+// thread); the two split each tile's 64 columns in halves, so that two warps per
+// sub-partition hide each other's latency.  An N = 64 score MMA costs nearly as
+// many cycles as an N = 128 one from a single issuing thread; from two threads
+// the two streams interleave, and a score buffer is complete once both have
+// committed to it.
 //
 // bwd_dq_tc: a 128-row query tile; Q and dO stay in shared memory and 64-key
 // tiles of K and V stream through a three-stage ring.  Per key tile j:
@@ -19,8 +23,9 @@
 //   dS_j (bf16) over S_j's columns once read                    (elementwise warps)
 //   dQ += dS_j K_j                   TS MMAs, N = 192: K_j read MN-major over its
 //                                    three 64-column panels
-// The MMA warp issues S_{j+1}, dP_{j+1} before dQ_j, so the tensor pipe works on
-// the next tile while the elementwise warps work on this one.
+// Warp 1 issues S_{j+1} before dQ_j, and warp 10 issues dP_{j+1} once the
+// elementwise warps are done with tile j - 1, so the tensor pipe works on the
+// next tile while the elementwise warps work on this one.
 // TMEM: S buffers [0,64) [64,128), dP buffers [128,192) [192,256), dQ [256,448).
 //
 // bwd_dkdv_tc: a 128-key tile; K and V stay in shared memory and 64-row tiles
@@ -28,8 +33,8 @@
 //   S^T_j = K Q_j^T, dP^T_j = V dO_j^T   SS MMAs, M = 128 keys, N = 64 rows
 //   P^T_j, dS^T_j (bf16) over S^T_j's columns once read            (elementwise)
 //   dV += P^T_j dO_j  (N = 128),  dK += dS^T_j Q_j  (N = 192)       TS MMAs
-// S^T has two buffers and dP^T one: dP^T_{j+1} goes out once the elementwise
-// warps have read dP^T_j.  TMEM: S^T [0,64) [64,128), dP^T [128,192),
+// S^T has two buffers and dP^T one: warp 10 issues dP^T_{j+1} once the
+// elementwise warps have read dP^T_j.  TMEM: S^T [0,64) [64,128), dP^T [128,192),
 // dV [192,320), dK [320,512).  The rope columns of dK are this head's share of
 // the head-shared k_rope gradient and are added into an fp32 accumulator.
 // Column ownership: the two warps of a lane quarter read 32 columns each of a
@@ -60,7 +65,7 @@ using tc::kWaitBudgetNs;
 using tc::range_bits;
 
 constexpr int kDn = 128, kDr = 64, kDqk = 192, kDv = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;           // warps 0..9 and a second MMA-issuing warp (warp 10)
 constexpr uint32_t kElemThreads = 256;  // warps 2..9
 constexpr uint32_t kStages = 3;
 constexpr uint32_t kTmemCols = 512;
@@ -82,7 +87,8 @@ enum {
   BAR_DPFREE = BAR_DS + 2,                // dkdv: dP^T read (256 arrivals)
   BAR_DONE = BAR_DPFREE + 1,              // all accumulating MMAs completed
   BAR_DRAIN = BAR_DONE + 1,
-  kNumBars = BAR_DRAIN + 1
+  BAR_DRAIN2 = BAR_DRAIN + 1,             // dkdv: the second MMA issuer's drain
+  kNumBars = BAR_DRAIN2 + 1
 };
 constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;
 constexpr uint32_t kOffAbort = kOffSlot + 4;
@@ -215,8 +221,11 @@ __device__ __forceinline__ Smem setup_smem(uint8_t* raw, const AttnParams& p) {
   return s;
 }
 
+// sp_commits: MMA commits that complete a score buffer (dkdv: S^T and dP^T
+// come from two issuing threads).
 __device__ __forceinline__ void init_common(const Smem& s, const CUtensorMap* m0, const CUtensorMap* m1,
-                                            const CUtensorMap* m2, const CUtensorMap* m3, const CUtensorMap* m4) {
+                                            const CUtensorMap* m2, const CUtensorMap* m3, const CUtensorMap* m4,
+                                            uint32_t sp_commits) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     ptx::mbar_init(s.ctl.bar(BAR_FIXED), 1);
@@ -225,12 +234,13 @@ __device__ __forceinline__ void init_common(const Smem& s, const CUtensorMap* m0
       ptx::mbar_init(s.ctl.bar(BAR_EMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(s.ctl.bar(BAR_SP + i), 1);
+      ptx::mbar_init(s.ctl.bar(BAR_SP + i), sp_commits);
       ptx::mbar_init(s.ctl.bar(BAR_DS + i), kElemThreads);
     }
     ptx::mbar_init(s.ctl.bar(BAR_DPFREE), kElemThreads);
     ptx::mbar_init(s.ctl.bar(BAR_DONE), 1);
     ptx::mbar_init(s.ctl.bar(BAR_DRAIN), 1);
+    ptx::mbar_init(s.ctl.bar(BAR_DRAIN2), 1);
     *s.ctl.abort = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -253,10 +263,10 @@ __device__ __forceinline__ void init_common(const Smem& s, const CUtensorMap* m0
 
 // The MMA thread's last act: wait (bounded) until every MMA it issued has
 // completed, so that TMEM can be released.
-__device__ __forceinline__ void drain(const Smem& s) {
-  ptx::tc_commit(s.ctl.bar(BAR_DRAIN));
+__device__ __forceinline__ void drain(const Smem& s, int bar = BAR_DRAIN) {
+  ptx::tc_commit(s.ctl.bar(bar));
   const uint64_t t0 = ptx::globaltimer();
-  while (!ptx::mbar_try_wait(s.ctl.bar(BAR_DRAIN), 0)) {
+  while (!ptx::mbar_try_wait(s.ctl.bar(bar), 0)) {
     if (ptx::globaltimer() - t0 > kWaitBudgetNs) {
       record_error(s.ctl.err, DFLASH_ERR_TIMEOUT);
       break;
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const auto tiles = tile_table(s.base, nkt, nkt, p.flag_tiles, tile_flags);
   tiles.build();
 
-  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV);  // its barrier publishes the flags
+  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV, 2);  // its barrier publishes the flags
   const uint32_t tmem = *s.tmem_slot;
   const uint32_t sQ = s.sbase + kOffFixed, sDO = sQ + 3 * kP128, sSt = s.sbase + kOffStage;
 
@@ -351,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA
-      const uint64_t dQd = ptx::smem_desc(sQ, 16, 1024), dDOd = ptx::smem_desc(sDO, 16, 1024);
+      const uint64_t dQd = ptx::smem_desc(sQ, 16, 1024);
       const uint64_t dStK = ptx::smem_desc(sSt, 16, 1024);   // stage, K-major (B of S and dP)
       const uint64_t dStN = ptx::smem_desc(sSt, kP64, 1024);  // stage, MN-major (B of dQ)
       bool ok = ctl.wait(BAR_FIXED, 0);
@@ -359,18 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = jj % kStages;
         if (!ctl.wait(BAR_FULL + st, (jj / kStages) & 1u)) return false;
         ptx::tc_fence_after();
-        const uint32_t dS = tmem + 64u * (jj & 1u), dP = tmem + 128u + 64u * (jj & 1u);
+        const uint32_t dS = tmem + 64u * (jj & 1u);
 #pragma unroll
         for (int ks = 0; ks < kDqk / 16; ++ks) {
           const uint32_t pn = ks >> 2, sub = (ks & 3) * 32;
           ptx::mma_ss(dS, dQd + ((pn * kP128 + sub) >> 4), dStK + ((st * kStageBytes + pn * kP64 + sub) >> 4),
                       kIdScore, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < kDv / 16; ++ks) {
-          const uint32_t pn = ks >> 2, sub = (ks & 3) * 32;
-          ptx::mma_ss(dP, dDOd + ((pn * kP128 + sub) >> 4),
-                      dStK + ((st * kStageBytes + (3 + pn) * kP64 + sub) >> 4), kIdScore, ks > 0);
         }
         ptx::tc_commit(ctl.bar(BAR_SP + (jj & 1u)));
         return true;
@@ -396,6 +400,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && j > 0) ok = issue_dq(j - 1);
       if (ok) ptx::tc_commit(ctl.bar(BAR_DONE));
       drain(s);
+    }
+  } else if (warp == 10) {
+    if (lane == 0) {
+      // ------------------------------------------------------ second MMA issuer: dP
+      const uint64_t dDOd = ptx::smem_desc(sDO, 16, 1024);
+      const uint64_t dStK = ptx::smem_desc(sSt, 16, 1024);
+      bool ok = ctl.wait(BAR_FIXED, 0);
+      uint32_t j = 0;
+      for (int kt = tiles.next(-1); ok && kt < nkt; kt = tiles.next(kt)) {
+        const uint32_t st = j % kStages;
+        if (!ctl.wait(BAR_FULL + st, (j / kStages) & 1u)) break;
+        // dP buffer j & 1 is free once the elementwise warps are done with tile j - 2
+        if (j > 1 && !ctl.wait(BAR_DS + (j & 1u), ((j - 2) >> 1) & 1u)) break;
+        ptx::tc_fence_after();
+        const uint32_t dP = tmem + 128u + 64u * (j & 1u);
+#pragma unroll
+        for (int ks = 0; ks < kDv / 16; ++ks) {
+          const uint32_t pn = ks >> 2, sub = (ks & 3) * 32;
+          ptx::mma_ss(dP, dDOd + ((pn * kP128 + sub) >> 4),
+                      dStK + ((st * kStageBytes + (3 + pn) * kP64 + sub) >> 4), kIdScore, ks > 0);
+        }
+        ptx::tc_commit(ctl.bar(BAR_SP + (j & 1u)));
+        ++j;
+      }
+      drain(s, BAR_DRAIN2);
     }
   } else {
     // ------------------------------------------------------------------ elementwise + epilogue
@@ -552,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const auto tiles = tile_table(s.base, nqt, nqt, p.flag_tiles, tile_flags);
   tiles.build();
 
-  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV);  // its barrier publishes the flags
+  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV, 2);  // its barrier publishes the flags
   const uint32_t tmem = *s.tmem_slot;
   const uint32_t sK = s.sbase + kOffFixed, sV = sK + 3 * kP128, sSt = s.sbase + kOffStage;
 
@@ -601,16 +630,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       dStK + ((st * kStageBytes + pn * kP64 + sub) >> 4), kIdScore, ks > 0);
         }
       };
-      auto issue_dpt = [&](uint32_t jj) {
-        const uint32_t st = jj % kStages;
-#pragma unroll
-        for (int ks = 0; ks < kDv / 16; ++ks) {
-          const uint32_t pn = ks >> 2, sub = (ks & 3) * 32;
-          ptx::mma_ss(tmem + 128u, dVd + ((pn * kP128 + sub) >> 4),
-                      dStK + ((st * kStageBytes + (3 + pn) * kP64 + sub) >> 4), kIdScore, ks > 0);
-        }
-        ptx::tc_commit(ctl.bar(BAR_SP + (jj & 1u)));
-      };
       auto issue_acc = [&](uint32_t jj) -> bool {
         const uint32_t st = jj % kStages;
         if (!ctl.wait(BAR_DS + (jj & 1u), (jj >> 1) & 1u)) return false;
@@ -626,6 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_commit(ctl.bar(BAR_EMPTY + st));
         return true;
       };
+      // S^T and the accumulating MMAs; warp 10 issues dP^T, so that the two
+      // streams of MMAs interleave and neither waits on the other's barrier.
       uint32_t j = 0;
       for (int t = tiles.next(-1); ok && t < nqt; t = tiles.next(t)) {
         if (!wait_stage(j)) {
@@ -633,15 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         issue_st(j);
-        if (j > 0) {
-          // dP^T has one buffer: the elementwise warps must have read dP^T(j-1)
-          if (!ctl.wait(BAR_DPFREE, (j - 1) & 1u)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-        }
-        issue_dpt(j);
+        ptx::tc_commit(ctl.bar(BAR_SP + (j & 1u)));
         if (j > 0 && !issue_acc(j - 1)) {
           ok = false;
           break;
@@ -651,6 +664,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && j > 0) ok = issue_acc(j - 1);
       if (ok) ptx::tc_commit(ctl.bar(BAR_DONE));
       drain(s);
+    }
+  } else if (warp == 10) {
+    if (lane == 0) {
+      // ------------------------------------------------------ second MMA issuer: dP^T
+      const uint64_t dVd = ptx::smem_desc(sV, 16, 1024);
+      const uint64_t dStK = ptx::smem_desc(sSt, 16, 1024);
+      bool ok = ctl.wait(BAR_FIXED, 0);
+      uint32_t j = 0;
+      for (int t = tiles.next(-1); ok && t < nqt; t = tiles.next(t)) {
+        const uint32_t st = j % kStages;
+        if (!ctl.wait(BAR_FULL + st, (j / kStages) & 1u)) break;
+        // dP^T has one buffer: the elementwise warps must have read dP^T(j-1)
+        if (j > 0 && !ctl.wait(BAR_DPFREE, (j - 1) & 1u)) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kDv / 16; ++ks) {
+          const uint32_t pn = ks >> 2, sub = (ks & 3) * 32;
+          ptx::mma_ss(tmem + 128u, dVd + ((pn * kP128 + sub) >> 4),
+                      dStK + ((st * kStageBytes + (3 + pn) * kP64 + sub) >> 4), kIdScore, ks > 0);
+        }
+        ptx::tc_commit(ctl.bar(BAR_SP + (j & 1u)));
+        ++j;
+      }
+      drain(s, BAR_DRAIN2);
     }
   } else {
     // ------------------------------------------------------------------ elementwise + epilogue
