@@ -75,6 +75,11 @@ constexpr uint32_t kStageBytes = 5 * kP64;  // dq: K (3 panels) + V (2); dkdv: Q
 constexpr uint32_t kOffFixed = 0;           // dq: Q (3 x 128 rows) + dO (2); dkdv: K (3) + V (2)
 constexpr uint32_t kOffStage = 5 * kP128;
 constexpr uint32_t kOffCols = kOffStage + kStages * kStageBytes;  // dkdv: per-warp column data
+// Epilogue staging in the idle stage ring: bytes per staged row (the row's bf16
+// results + 16 of padding, so that the 32 lanes' row writes spread over the banks).
+constexpr uint32_t kStgRow = 336;    // dkdv: 320 (dv + 32 columns of dk_nope, or 96 columns of dk_nope)
+constexpr uint32_t kStgRowDq = 208;  // dq: 192 (96 columns)
+static_assert(8 * 32 * kStgRow <= kStages * kStageBytes, "epilogue staging fits in the stage ring");
 constexpr uint32_t kColWords = 5 * 32;                             // per warp: lse2, D, ctx, nlo, nhi
 constexpr uint32_t kOffBar = kOffCols + 8 * kColWords * 4;
 
@@ -519,12 +524,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(ctl.bar(BAR_DS + (j & 1u)));
       ++j;
     }
-    // ---- epilogue: dq = scale * dQ (bf16); each warp of a lane quarter writes 96 of the 192 columns
+    // ---- epilogue: dq = scale * dQ (bf16); each warp of a lane quarter writes 96 of the 192 columns.
+    // The rows of a warp lie H * 384 bytes apart in dq: the results are staged in
+    // the idle stage ring and written row by row (12 lanes to a row's 192 bytes).
     if (ok && j > 0 && !__all_sync(0xffffffffu, ctl.wait(BAR_DONE, 0))) ok = false;
     if (ok) {
       ptx::tc_fence_after();
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) +
-                                            (((long long)b * Q + (row_ok ? i : 0)) * p.H + h) * (long long)kDqk);
+      uint8_t* stg = s.base + kOffStage + (uint32_t)(warp - 2) * 32u * kStgRowDq;
 #pragma unroll 1
       for (int cc = 96 * (int)half; cc < 96 * (int)half + 96; cc += 32) {
         uint32_t o[32], pk[16];
@@ -538,10 +544,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 2)
           pk[e / 2] = ptx::pack_bf16x2(__uint_as_float(o[e]) * p.scale, __uint_as_float(o[e + 1]) * p.scale);
-        if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(stg + lane * kStgRowDq + (cc - 96 * (int)half) * 2);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[cc / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-        }
+        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      }
+      __syncwarp();
+      constexpr int kPieces = 96 / 8;  // 16-byte pieces of a row's 96 columns
+      for (int idx = lane; idx < 32 * kPieces; idx += 32) {
+        const int r = idx / kPieces, pc = idx % kPieces;
+        const int ir = r0 + quad * 32 + r;
+        if (ir >= Q) continue;
+        __nv_bfloat16* g = static_cast<__nv_bfloat16*>(a.dq) + (((long long)b * Q + ir) * p.H + h) * (long long)kDqk;
+        *reinterpret_cast<uint4*>(g + 96 * (int)half + 8 * pc) =
+            *reinterpret_cast<const uint4*>(stg + r * kStgRowDq + 16 * pc);
       }
     }
   }
@@ -825,12 +840,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue: dv, dk_nope (bf16), rope share of dk added into the fp32 accumulator.
     // TMEM columns 192.. hold dV (128) then dK (192): ten 32-column chunks, five per warp.
+    // A thread holds one key row, and the rows of a warp lie H * 256 bytes apart
+    // in dv and dk_nope: the bf16 results are staged in the idle stage ring and
+    // written row by row, 16 lanes to a 256-byte row, so that a store covers two
+    // rows instead of 32.
     if (ok && j > 0 && !__all_sync(0xffffffffu, ctl.wait(BAR_DONE, 0))) ok = false;
     if (ok) {
       ptx::tc_fence_after();
+      uint8_t* stg = s.base + kOffStage + (uint32_t)(warp - 2) * 32u * kStgRow;
       const long long kk = (long long)b * K + (key_ok ? k : 0);
-      uint4* dvd = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dvo) + (kk * p.H + h) * (long long)kDv);
-      uint4* dkd = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dkn) + (kk * p.H + h) * (long long)kDn);
       float4* racc = reinterpret_cast<float4*>(a.dkr_acc + kk * (long long)kDr);
 #pragma unroll 1
       for (int cc = 160 * (int)half; cc < 160 * (int)half + 160; cc += 32) {
@@ -842,17 +860,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
-        if (!key_ok) continue;
         if (cc < kDv + kDn) {
           const float sc = cc < kDv ? 1.f : p.scale;
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
             pk[e / 2] = ptx::pack_bf16x2(__uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc);
-          uint4* dst = cc < kDv ? dvd + cc / 8 : dkd + (cc - kDv) / 8;
+          // staged row: half 0 [dv 0..127 | dk_nope 0..31], half 1 [dk_nope 32..127]
+          uint4* dst = reinterpret_cast<uint4*>(stg + lane * kStgRow + (cc - 160 * (int)half) * 2);
 #pragma unroll
           for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-        } else if (j > 0) {
+        } else if (j > 0 && key_ok) {
           const int d0 = cc - kDv - kDn;
 #pragma unroll
           for (int v = 0; v < 8; ++v)
@@ -860,6 +878,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                       make_float4(__uint_as_float(o[4 * v]) * p.scale, __uint_as_float(o[4 * v + 1]) * p.scale,
                                   __uint_as_float(o[4 * v + 2]) * p.scale, __uint_as_float(o[4 * v + 3]) * p.scale));
         }
+      }
+      __syncwarp();
+      // staged bytes [soff, soff + 16 * pieces) of each row -> columns gcol.. of out
+      auto put = [&](uint32_t soff, int pieces, void* out, int ld, int gcol) {
+        for (int idx = lane; idx < 32 * pieces; idx += 32) {
+          const int r = idx / pieces, pc = idx % pieces;
+          const int kr = k0 + quad * 32 + r;
+          if (kr >= K) continue;
+          __nv_bfloat16* g = static_cast<__nv_bfloat16*>(out) + (((long long)b * K + kr) * p.H + h) * (long long)ld;
+          *reinterpret_cast<uint4*>(g + gcol + 8 * pc) = *reinterpret_cast<const uint4*>(stg + r * kStgRow + soff + 16 * pc);
+        }
+      };
+      if (half == 0) {
+        put(0, kDv / 8, a.dvo, kDv, 0);
+        put(2 * kDv, 4, a.dkn, kDn, 0);
+      } else {
+        put(0, (kDn - 32) / 8, a.dkn, kDn, 32);
       }
     }
   }
