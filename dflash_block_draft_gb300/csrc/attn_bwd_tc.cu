@@ -226,37 +226,38 @@ __device__ __forceinline__ Smem setup_smem(uint8_t* raw, const AttnParams& p) {
   return s;
 }
 
-// sp_commits: MMA commits that complete a score buffer (dkdv: S^T and dP^T
-// come from two issuing threads).
-__device__ __forceinline__ void init_common(const Smem& s, const CUtensorMap* m0, const CUtensorMap* m1,
-                                            const CUtensorMap* m2, const CUtensorMap* m3, const CUtensorMap* m4,
-                                            uint32_t sp_commits) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    ptx::mbar_init(s.ctl.bar(BAR_FIXED), 1);
-    for (uint32_t i = 0; i < kStages; ++i) {
-      ptx::mbar_init(s.ctl.bar(BAR_FULL + i), 1);
-      ptx::mbar_init(s.ctl.bar(BAR_EMPTY + i), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(s.ctl.bar(BAR_SP + i), sp_commits);
-      ptx::mbar_init(s.ctl.bar(BAR_DS + i), kElemThreads);
-    }
-    ptx::mbar_init(s.ctl.bar(BAR_DPFREE), kElemThreads);
-    ptx::mbar_init(s.ctl.bar(BAR_DONE), 1);
-    ptx::mbar_init(s.ctl.bar(BAR_DRAIN), 1);
-    ptx::mbar_init(s.ctl.bar(BAR_DRAIN2), 1);
-    *s.ctl.abort = 0;
-    ptx::fence_mbar_init();
-    ptx::fence_proxy_async_smem();
+// Thread 0, first: the barriers (sp_commits: MMA commits that complete a score
+// buffer, two since S and dP come from two issuing threads) and the tensor maps.
+__device__ __forceinline__ void init_barriers(const Smem& s, const CUtensorMap* m0, const CUtensorMap* m1,
+                                              const CUtensorMap* m2, const CUtensorMap* m3, const CUtensorMap* m4,
+                                              uint32_t sp_commits) {
+  ptx::mbar_init(s.ctl.bar(BAR_FIXED), 1);
+  for (uint32_t i = 0; i < kStages; ++i) {
+    ptx::mbar_init(s.ctl.bar(BAR_FULL + i), 1);
+    ptx::mbar_init(s.ctl.bar(BAR_EMPTY + i), 1);
   }
-  if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(m0);
-    ptx::prefetch_tmap(m1);
-    ptx::prefetch_tmap(m2);
-    ptx::prefetch_tmap(m3);
-    ptx::prefetch_tmap(m4);
+  for (int i = 0; i < 2; ++i) {
+    ptx::mbar_init(s.ctl.bar(BAR_SP + i), sp_commits);
+    ptx::mbar_init(s.ctl.bar(BAR_DS + i), kElemThreads);
   }
+  ptx::mbar_init(s.ctl.bar(BAR_DPFREE), kElemThreads);
+  ptx::mbar_init(s.ctl.bar(BAR_DONE), 1);
+  ptx::mbar_init(s.ctl.bar(BAR_DRAIN), 1);
+  ptx::mbar_init(s.ctl.bar(BAR_DRAIN2), 1);
+  *s.ctl.abort = 0;
+  ptx::fence_mbar_init();
+  ptx::fence_proxy_async_smem();
+  ptx::prefetch_tmap(m0);
+  ptx::prefetch_tmap(m1);
+  ptx::prefetch_tmap(m2);
+  ptx::prefetch_tmap(m3);
+  ptx::prefetch_tmap(m4);
+}
+
+// All threads, after the tile table is built: TMEM, and the barrier that
+// publishes the barriers' initialisation and the table.
+__device__ __forceinline__ void init_common(const Smem& s) {
+  const int warp = threadIdx.x >> 5;
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(s.tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
@@ -332,20 +333,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!DENSE) return need;
     return need | (p.classes[((long long)b * p.nqt + t) * p.nkt + (kt * 64) / kTileN] == DFLASH_TILE_FULL ? 2u : 0u);
   };
+  const uint32_t sQ = s.sbase + kOffFixed, sDO = sQ + 3 * kP128, sSt = s.sbase + kOffStage;
+  if (threadIdx.x == 0) {
+    init_barriers(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV, 2);
+    // the resident Q and dO need no tile table: they load while it is built
+    const int qrow = (int)((long long)b * Q + r0);
+    ptx::mbar_arrive_expect_tx(ctl.bar(BAR_FIXED), 5 * kP128);
+    for (int pn = 0; pn < 3; ++pn) ptx::tma_load_3d(sQ + pn * kP128, &tmQ, ctl.bar(BAR_FIXED), 64 * pn, h, qrow);
+    for (int pn = 0; pn < 2; ++pn) ptx::tma_load_3d(sDO + pn * kP128, &tmDO, ctl.bar(BAR_FIXED), 64 * pn, h, qrow);
+  }
   const auto tiles = tile_table(s.base, nkt, nkt, p.flag_tiles, tile_flags);
   tiles.build();
 
-  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV, 2);  // its barrier publishes the flags
+  init_common(s);  // its barrier publishes the barriers and the flags
   const uint32_t tmem = *s.tmem_slot;
-  const uint32_t sQ = s.sbase + kOffFixed, sDO = sQ + 3 * kP128, sSt = s.sbase + kOffStage;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA
-      const int qrow = (int)((long long)b * Q + r0);
-      ptx::mbar_arrive_expect_tx(ctl.bar(BAR_FIXED), 5 * kP128);
-      for (int pn = 0; pn < 3; ++pn) ptx::tma_load_3d(sQ + pn * kP128, &tmQ, ctl.bar(BAR_FIXED), 64 * pn, h, qrow);
-      for (int pn = 0; pn < 2; ++pn) ptx::tma_load_3d(sDO + pn * kP128, &tmDO, ctl.bar(BAR_FIXED), 64 * pn, h, qrow);
       uint32_t j = 0;
       // (timeout test: the stalled CTA's key tiles never arrive)
       for (int kt = tiles.next(-1); kt < nkt && (int)blockIdx.x != p.stall_cta; kt = tiles.next(kt)) {
@@ -593,23 +598,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     return (pair_needed(a, b, t * 64, min(t * 64 + 64, Q), k0, k1, amax) ? 1u : 0u) |
            (whole && k1 <= S && k1 <= amin ? 2u : 0u);
   };
+  const uint32_t sK = s.sbase + kOffFixed, sV = sK + 3 * kP128, sSt = s.sbase + kOffStage;
+  if (threadIdx.x == 0) {
+    init_barriers(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV, 2);
+    // the resident K and V need no tile table: they load while it is built
+    const int krow = (int)((long long)b * K + k0);
+    ptx::mbar_arrive_expect_tx(ctl.bar(BAR_FIXED), 5 * kP128);
+    ptx::tma_load_3d(sK, &tmKn, ctl.bar(BAR_FIXED), 0, h, krow);
+    ptx::tma_load_3d(sK + kP128, &tmKn, ctl.bar(BAR_FIXED), 64, h, krow);
+    ptx::tma_load_2d(sK + 2 * kP128, &tmKr, ctl.bar(BAR_FIXED), 0, krow);
+    ptx::tma_load_3d(sV, &tmV, ctl.bar(BAR_FIXED), 0, h, krow);
+    ptx::tma_load_3d(sV + kP128, &tmV, ctl.bar(BAR_FIXED), 64, h, krow);
+  }
   const auto tiles = tile_table(s.base, nqt, nqt, p.flag_tiles, tile_flags);
   tiles.build();
 
-  init_common(s, &tmQ, &tmDO, &tmKn, &tmKr, &tmV, 2);  // its barrier publishes the flags
+  init_common(s);  // its barrier publishes the barriers and the flags
   const uint32_t tmem = *s.tmem_slot;
-  const uint32_t sK = s.sbase + kOffFixed, sV = sK + 3 * kP128, sSt = s.sbase + kOffStage;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA
-      const int krow = (int)((long long)b * K + k0);
-      ptx::mbar_arrive_expect_tx(ctl.bar(BAR_FIXED), 5 * kP128);
-      ptx::tma_load_3d(sK, &tmKn, ctl.bar(BAR_FIXED), 0, h, krow);
-      ptx::tma_load_3d(sK + kP128, &tmKn, ctl.bar(BAR_FIXED), 64, h, krow);
-      ptx::tma_load_2d(sK + 2 * kP128, &tmKr, ctl.bar(BAR_FIXED), 0, krow);
-      ptx::tma_load_3d(sV, &tmV, ctl.bar(BAR_FIXED), 0, h, krow);
-      ptx::tma_load_3d(sV + kP128, &tmV, ctl.bar(BAR_FIXED), 64, h, krow);
       uint32_t j = 0;
       // (timeout test: the stalled CTA's query tiles never arrive)
       for (int t = tiles.next(-1); t < nqt && (int)blockIdx.x != p.stall_cta; t = tiles.next(t)) {
