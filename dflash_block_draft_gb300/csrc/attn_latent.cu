@@ -270,8 +270,11 @@ cudaError_t launch_head_gemm(const GemmArgs& g, const CUtensorMap& mA, const CUt
 // Latent attention (tensor cores).
 // Unit = (request, split of kLSplit key tiles, group of kLHeads heads): 64
 // query rows, row n = 4 * token + head-in-group (the TMA box order of q_abs).
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner (warps 2, 3 idle), warps 4..11 softmax and epilogue -- two warps per
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer (QK, and
+// PV of latent blocks 0, 1) and TMEM owner, warp 2 the PV issuer of latent
+// blocks 2, 3 (two issuing threads interleave their N = 64 MMAs; the PV
+// barriers complete on both commits), warp 3 idle, warps 4..11 softmax and
+// epilogue -- two warps per
 // TMEM lane quarter (keys 32q..32q+31), each owning 32 of the 64 rows.  The
 // control warpgroup gives registers back (setmaxnreg 104) so that the softmax
 // warps get 200: 128*104 + 256*200 = 384*168, the launch budget.
@@ -316,7 +319,8 @@ enum {
   LB_PV_DONE = LB_P_HI + 1,    // one phase per tile
   LB_O_FULL = LB_PV_DONE + 1,
   LB_DRAIN = LB_O_FULL + 1,
-  kLBars = LB_DRAIN + 1
+  LB_DRAIN2 = LB_DRAIN + 1,    // the second PV issuer's drain
+  kLBars = LB_DRAIN2 + 1
 };
 constexpr uint32_t kLOffSlot = kLOffBar + 8 * kLBars;
 constexpr uint32_t kLOffAbort = kLOffSlot + 4;
@@ -425,11 +429,12 @@ __global__ void __launch_bounds__(kLThreads, 1)
     }
     ptx::mbar_init(ctl.bar(LB_S_FULL), 1);
     ptx::mbar_init(ctl.bar(LB_P_LO), 128);
-    ptx::mbar_init(ctl.bar(LB_P_FREE), 1);
+    ptx::mbar_init(ctl.bar(LB_P_FREE), 2);  // both PV issuers
     ptx::mbar_init(ctl.bar(LB_P_HI), 128);
-    ptx::mbar_init(ctl.bar(LB_PV_DONE), 1);
-    ptx::mbar_init(ctl.bar(LB_O_FULL), 1);
+    ptx::mbar_init(ctl.bar(LB_PV_DONE), 2);
+    ptx::mbar_init(ctl.bar(LB_O_FULL), 2);
     ptx::mbar_init(ctl.bar(LB_DRAIN), 1);
+    ptx::mbar_init(ctl.bar(LB_DRAIN2), 1);
     *ctl.abort = 0;
     for (int i = 0; i < 9; ++i) vote[i] = 0u;
     ptx::fence_mbar_init();
@@ -490,7 +495,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
       if (n > 0) ctl.wait_landed(LB_Q_FULL, (n - 1) & 1u);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer (QK, PV of blocks 0, 1)
     if (lane == 0) {
       uint32_t g = 0, n = 0;
       bool stop = false;
@@ -533,7 +538,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
           }
           ptx::tc_fence_after();
 #pragma unroll 1
-          for (int m = 0; m < 4; ++m) {
+          for (int m = 0; m < 2; ++m) {  // latent blocks 0, 1 (warp 2 issues 2, 3)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
               ptx::mma_ss(tmem + kLColO + 64u * m, ptx::smem_desc(sK + 2 * m * kLKPanel + ks * 2048, kLKPanel, 1024),
@@ -546,7 +551,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
           }
           ptx::tc_fence_after();
 #pragma unroll 1
-          for (int m = 0; m < 4; ++m) {
+          for (int m = 0; m < 2; ++m) {
 #pragma unroll
             for (int ks = 4; ks < 8; ++ks)
               ptx::mma_ss(tmem + kLColO + 64u * m, ptx::smem_desc(sK + 2 * m * kLKPanel + ks * 2048, kLKPanel, 1024),
@@ -565,6 +570,61 @@ __global__ void __launch_bounds__(kLThreads, 1)
       }
       ptx::tc_commit(ctl.bar(LB_DRAIN));
       ctl.wait_landed(LB_DRAIN, 0);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ second PV issuer
+    // O^T of latent blocks 2 and 3, so that the two streams of N = 64 MMAs
+    // interleave; it follows the units and tiles of warp 1.
+    if (lane == 0) {
+      uint32_t g = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+        const LUnit it = latent_unit(a, u);
+        if (!it.ok) continue;
+        int kt = lnext_tile(a, it, it.kt0 - 1);
+        if (kt >= it.kt1) continue;
+        bool first = true;
+        const uint32_t sP = sbase + kLOffP;
+        for (;;) {
+          const int kn = lnext_tile(a, it, kt);
+          if (!ctl.wait(LB_P_LO, g & 1u)) {
+            stop = true;
+            break;
+          }
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int m = 2; m < 4; ++m) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              ptx::mma_ss(tmem + kLColO + 64u * m, ptx::smem_desc(sK + 2 * m * kLKPanel + ks * 2048, kLKPanel, 1024),
+                          ptx::smem_desc(sP + ks * 32, 16, 1024), kLIdPV, !(first && ks == 0));
+          }
+          ptx::tc_commit(ctl.bar(LB_P_FREE));
+          if (!ctl.wait(LB_P_HI, g & 1u)) {
+            stop = true;
+            break;
+          }
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int m = 2; m < 4; ++m) {
+#pragma unroll
+            for (int ks = 4; ks < 8; ++ks)
+              ptx::mma_ss(tmem + kLColO + 64u * m, ptx::smem_desc(sK + 2 * m * kLKPanel + ks * 2048, kLKPanel, 1024),
+                          ptx::smem_desc(sP + (ks - 4) * 32, 16, 1024), kLIdPV, 1u);
+            ptx::tc_commit(ctl.bar(LB_SLOT_EMPTY + 2 * m));
+            ptx::tc_commit(ctl.bar(LB_SLOT_EMPTY + 2 * m + 1));
+          }
+          ptx::tc_commit(ctl.bar(LB_PV_DONE));
+          first = false;
+          ++g;
+          if (kn >= it.kt1) break;
+          kt = kn;
+        }
+        if (stop) break;
+        ptx::tc_commit(ctl.bar(LB_O_FULL));
+      }
+      ptx::tc_commit(ctl.bar(LB_DRAIN2));
+      ctl.wait_landed(LB_DRAIN2, 0);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue (warps 4..11)
