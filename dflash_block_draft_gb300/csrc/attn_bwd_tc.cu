@@ -785,13 +785,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // anchored: which of the warp's 32 rows see this thread's key, as a bit mask
       // worked out before the scores arrive (one short loop, so that the element
       // loop below carries no per-element selection code)
+      // (16-byte loads of four rows' bounds, no branches: rows past Q were staged
+      // with empty ranges)
       uint32_t vmask = 0xffffffffu;
       if (!DENSE && !full_tile) {
         vmask = 0u;
         if (key_ok) {
-#pragma unroll 4
-          for (int col = 0; col < 32; ++col)
-            vmask |= (r0 + col < Q && (k < cctx[col] || (k >= cnlo[col] && k < cnhi[col])) ? 1u : 0u) << col;
+          const int4* c4 = reinterpret_cast<const int4*>(cctx);
+          const int4* l4 = reinterpret_cast<const int4*>(cnlo);
+          const int4* h4 = reinterpret_cast<const int4*>(cnhi);
+#pragma unroll 2
+          for (int v = 0; v < 8; ++v) {
+            const int4 c = c4[v], lo = l4[v], hi = h4[v];
+            const uint32_t b0 = (uint32_t)((k < c.x) | ((k >= lo.x) & (k < hi.x)));
+            const uint32_t b1 = (uint32_t)((k < c.y) | ((k >= lo.y) & (k < hi.y)));
+            const uint32_t b2 = (uint32_t)((k < c.z) | ((k >= lo.z) & (k < hi.z)));
+            const uint32_t b3 = (uint32_t)((k < c.w) | ((k >= lo.w) & (k < hi.w)));
+            vmask |= (b0 | (b1 << 1) | (b2 << 2) | (b3 << 3)) << (4 * v);
+          }
         }
       }
       if (!__all_sync(0xffffffffu, ctl.wait(BAR_SP + (j & 1u), (j >> 1) & 1u))) {
