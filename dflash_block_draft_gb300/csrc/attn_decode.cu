@@ -351,6 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kt = next_tile(a, it, it.kt0 - 1); kt < it.kt1; kt = next_tile(a, it, kt), ++g) {
         const int key = kt * kBN + t;  // this thread's key, relative to the request
         const bool full = unit_class(a, it, kt) == DFLASH_TILE_FULL && kt * kBN + kBN <= K;
+        // Which rows see this thread's key, as a bit mask worked out before the
+        // scores arrive, without branches (rows past Qn hold empty ranges).
+        uint32_t vmask = (1u << Qn) - 1u;
+        if (!full) {
+          vmask = 0u;
+#pragma unroll
+          for (int q = 0; q < kQN; ++q)
+            vmask |= (uint32_t)((key < s_ctx[q]) | ((key >= s_ctx[kQN + q]) & (key < s_ctx[2 * kQN + q]))) << q;
+        }
         if (!ctl.wait(BAR_S_FULL + (g & 1u), (g >> 1) & 1u)) {
           stop = true;
           break;
@@ -362,9 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t flags = 0;
 #pragma unroll
         for (int q = 0; q < kQN; ++q) {
-          bool vis = full ? q < Qn : false;
-          if (!full && q < Qn) vis = key < s_ctx[q] || (key >= s_ctx[kQN + q] && key < s_ctx[2 * kQN + q]);
-          x[q] = vis ? x[q] * c2 : -INFINITY;
+          x[q] = (vmask >> q) & 1u ? x[q] * c2 : -INFINITY;
           if (x[q] > m_ref[q] + 8.0f) flags |= 1u << q;
         }
         // Does any of the 128 keys move some row's reference maximum?

@@ -667,6 +667,17 @@ __global__ void __launch_bounds__(kLThreads, 1)
         const bool full = lunit_class(a, it, kt) == DFLASH_TILE_FULL && kt * kLBN + kLBN <= K;
         // The wait result is made warp-uniform (TMEM loads are warp-collective)
         // and then group-uniform through the vote words (named barriers follow).
+        // which of the half's 32 rows see this thread's key, worked out before the
+        // scores arrive and without branches (four rows per draft token)
+        uint32_t vmask = rows_valid;
+        if (!full) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int t = 8 * hf + u;
+            const uint32_t v = (uint32_t)((key < s_ctx[t]) | ((key >= s_ctx[kLTok + t]) & (key < s_ctx[2 * kLTok + t])));
+            vmask &= ~((v ^ 1u) * (0xFu << (4 * u)));
+          }
+        }
         const bool ok = __all_sync(0xffffffffu, ctl.wait(LB_S_FULL, g & 1u));
         float x[32];
         uint32_t flags = 0;
@@ -674,15 +685,6 @@ __global__ void __launch_bounds__(kLThreads, 1)
           ptx::tc_fence_after();
           ptx::tmem_ld32(tmem + lane_off + kLColS + 32u * hf, reinterpret_cast<uint32_t*>(x));
           ptx::tmem_wait_ld();
-          uint32_t vmask = rows_valid;
-          if (!full) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int t = 8 * hf + u;
-              const bool v = key < s_ctx[t] || (key >= s_ctx[kLTok + t] && key < s_ctx[2 * kLTok + t]);
-              if (!v) vmask &= ~(0xFu << (4 * u));
-            }
-          }
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             x[c] = (vmask >> c) & 1u ? x[c] * c2 : -INFINITY;
