@@ -87,12 +87,12 @@ enum {
   BAR_FIXED = 0,                          // Q+dO (dq) or K+V (dkdv) landed
   BAR_FULL = 1,                           // kStages: stage landed
   BAR_EMPTY = BAR_FULL + kStages,         // kStages: stage free
-  BAR_SP = BAR_EMPTY + kStages,           // 2: scores of buffer b computed
+  BAR_SP = BAR_EMPTY + kStages,           // 2: scores of buffer b computed (S and dP: two commits)
   BAR_DS = BAR_SP + 2,                    // 2: bf16 operands of buffer b written (256 arrivals)
   BAR_DPFREE = BAR_DS + 2,                // dkdv: dP^T read (256 arrivals)
   BAR_DONE = BAR_DPFREE + 1,              // all accumulating MMAs completed
   BAR_DRAIN = BAR_DONE + 1,
-  BAR_DRAIN2 = BAR_DRAIN + 1,             // dkdv: the second MMA issuer's drain
+  BAR_DRAIN2 = BAR_DRAIN + 1,             // the second MMA issuer's drain
   kNumBars = BAR_DRAIN2 + 1
 };
 constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;
