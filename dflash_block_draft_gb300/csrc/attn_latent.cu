@@ -30,7 +30,7 @@
 //    unit holds 64 query rows (4 heads x 16 draft tokens) against 128-key
 //    tiles: S^T = K_tile Q^T (M = 128 keys, N = 64 rows, K = 576) and
 //    O^T += C_tile^T P^T (M = 4 x 128 latent dims, N = 64, K = 128 keys),
-//    accumulated in TMEM.  The context is split into units of kSplitTiles key
+//    accumulated in TMEM.  The context is split into units of kLSplit key
 //    tiles whose normalised partials are merged by a log-sum-exp combine.
 #include <math.h>
 #include <string.h>
