@@ -805,6 +805,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // dense, partial tile: the warp's 32 rows' mask values at this thread's key
+      // (bf16 pairs), loaded before the scores arrive
+      uint32_t mpk[16];
+      if (DENSE && !full_tile) {
+        const uint16_t* mk = static_cast<const uint16_t*>(p.mask) + (long long)b * Q * K + k;
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const uint32_t lo = key_ok && r0 + c < Q ? mk[(long long)(r0 + c) * K] : 0xFF80u;
+          const uint32_t hi = key_ok && r0 + c + 1 < Q ? mk[(long long)(r0 + c + 1) * K] : 0xFF80u;
+          mpk[c / 2] = lo | (hi << 16);
+        }
+      }
       if (!__all_sync(0xffffffffu, ctl.wait(BAR_SP + (j & 1u), (j >> 1) & 1u))) {
         ok = false;
         break;
@@ -837,10 +849,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             arg = fmaf(x, c2, nl[col]);
             vis = true;
           } else {
-            const int i = r0 + col;
-            float m2 = -INFINITY;
-            if (key_ok && i < Q)
-              m2 = mask2(__bfloat162float(static_cast<const __nv_bfloat16*>(p.mask)[((long long)b * Q + i) * K + k]));
+            const uint32_t w = mpk[col / 2];
+            const float m2 = mask2(__uint_as_float((col & 1) ? (w & 0xFFFF0000u) : (w << 16)));
             vis = m2 != -INFINITY;
             arg = fmaf(x, c2, m2) + nl[col];
           }
