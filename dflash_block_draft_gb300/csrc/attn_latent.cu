@@ -270,11 +270,12 @@ cudaError_t launch_head_gemm(const GemmArgs& g, const CUtensorMap& mA, const CUt
 // Latent attention (tensor cores).
 // Unit = (request, split of kLSplit key tiles, group of kLHeads heads): 64
 // query rows, row n = 4 * token + head-in-group (the TMA box order of q_abs).
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer (QK, and
-// PV of latent blocks 0, 1) and TMEM owner, warp 2 the PV issuer of latent
-// blocks 2, 3 (two issuing threads interleave their N = 64 MMAs; the PV
-// barriers complete on both commits), warp 3 idle, warps 4..11 softmax and
-// epilogue -- two warps per
+// Warp roles (384 threads): warp 0 TMA producer; warp 1 TMEM owner and MMA
+// issuer of QK over latent panels 0-3 and the rope panel and of PV for latent
+// blocks 0, 1; warp 2 the MMA issuer of QK over latent panels 4-7 (its own S^T
+// accumulator, which the softmax adds) and of PV for blocks 2, 3 -- two issuing
+// threads interleave their N = 64 MMAs, and the S and PV barriers complete on
+// both commits; warp 3 idle; warps 4..11 softmax and epilogue -- two warps per
 // TMEM lane quarter (keys 32q..32q+31), each owning 32 of the 64 rows.  The
 // control warpgroup gives registers back (setmaxnreg 104) so that the softmax
 // warps get 200: 128*104 + 256*200 = 384*168, the launch budget.
@@ -287,8 +288,8 @@ cudaError_t launch_head_gemm(const GemmArgs& g, const CUtensorMap& mA, const CUt
 // as soon as QK of a tile completes, and the next tile's rope panel loads
 // while this tile's softmax and PV run; each latent slot is refilled as soon
 // as the second-half PV reading it completes.
-// TMEM: S^T [0,64) (128 keys x 64 rows), O^T blocks [64 + 64m, +64), m < 4
-// (128 latent dims x 64 rows each).
+// TMEM: S^T [0,64) and [320,384) (128 keys x 64 rows, the two halves of the QK
+// contraction), O^T blocks [64 + 64m, +64), m < 4 (128 latent dims x 64 rows each).
 // ============================================================================
 constexpr int kLRank = 512, kLDr = 64;
 constexpr int kLPanels = (kLRank + kLDr) / 64;  // 9
@@ -329,7 +330,8 @@ constexpr uint32_t kLRedWords = 4 * kLRows + 9 + 3 * kLTok;  // maxima/sums [4][
 constexpr uint32_t kLSmem = kLOffRed + 4 * kLRedWords + 1024;
 static_assert(kLSmem <= 232448, "shared memory budget");
 constexpr uint32_t kLTmemCols = 512;
-constexpr uint32_t kLColS = 0, kLColO = 64;
+constexpr uint32_t kLColS = 0, kLColO = 64, kLColS2 = 320;  // S^T: latent panels 0-3 + rope, and 4-7
+constexpr int kLQkSplit = 4;  // QK: warp 1 takes latent panels 0-3 and the rope panel, warp 2 panels 4-7
 constexpr int kLThreads = 384;
 constexpr int kLLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
 constexpr uint32_t kLCtlRegs = 104, kLSoftRegs = 200;
@@ -422,12 +424,12 @@ __global__ void __launch_bounds__(kLThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ctl.bar(LB_Q_FULL), 1);
-    ptx::mbar_init(ctl.bar(LB_Q_EMPTY), 1);
+    ptx::mbar_init(ctl.bar(LB_Q_EMPTY), 2);  // both QK issuers
     for (int s = 0; s < kLPanels; ++s) {
       ptx::mbar_init(ctl.bar(LB_SLOT_FULL + s), 1);
       ptx::mbar_init(ctl.bar(LB_SLOT_EMPTY + s), 1);
     }
-    ptx::mbar_init(ctl.bar(LB_S_FULL), 1);
+    ptx::mbar_init(ctl.bar(LB_S_FULL), 2);
     ptx::mbar_init(ctl.bar(LB_P_LO), 128);
     ptx::mbar_init(ctl.bar(LB_P_FREE), 2);  // both PV issuers
     ptx::mbar_init(ctl.bar(LB_P_HI), 128);
@@ -495,7 +497,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
       if (n > 0) ctl.wait_landed(LB_Q_FULL, (n - 1) & 1u);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (QK, PV of blocks 0, 1)
+    // ------------------------------------------------------------ MMA issuer (QK of panels 0-3 + rope, PV of blocks 0, 1)
     if (lane == 0) {
       uint32_t g = 0, n = 0;
       bool stop = false;
@@ -514,7 +516,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
           const int kn = lnext_tile(a, it, kt);
           // S^T = K_tile Q^T.  S^T is free: the softmax read S^T of the previous
           // tile before its P^T arrival, which PV of that tile waited for.
-          for (int pn = 0; pn < kLPanels && !stop; ++pn) {
+          for (int ip = 0; ip <= kLQkSplit && !stop; ++ip) {
+            const int pn = ip < kLQkSplit ? ip : kLPanels - 1;  // latent 0..3, then rope
             if (!ctl.wait(LB_SLOT_FULL + pn, g & 1u)) {
               stop = true;
               break;
@@ -523,7 +526,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
               ptx::mma_ss(tmem + kLColS, ptx::smem_desc(sK + pn * kLKPanel + ks * 32, 16, 1024),
-                          ptx::smem_desc(sQ + pn * kLQPanel + ks * 32, 16, 1024), kLIdQK, (pn | ks) != 0);
+                          ptx::smem_desc(sQ + pn * kLQPanel + ks * 32, 16, 1024), kLIdQK, (ip | ks) != 0);
           }
           if (stop) break;
           ptx::tc_commit(ctl.bar(LB_S_FULL));
@@ -572,21 +575,42 @@ __global__ void __launch_bounds__(kLThreads, 1)
       ctl.wait_landed(LB_DRAIN, 0);
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------ second PV issuer
-    // O^T of latent blocks 2 and 3, so that the two streams of N = 64 MMAs
-    // interleave; it follows the units and tiles of warp 1.
+    // ------------------------------------------------------------ second MMA issuer
+    // QK of latent panels 4-7 and O^T of latent blocks 2 and 3, so that the two
+    // streams of N = 64 MMAs interleave; it follows the units and tiles of warp 1.
     if (lane == 0) {
-      uint32_t g = 0;
+      uint32_t g = 0, n = 0;
       bool stop = false;
       for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
         const LUnit it = latent_unit(a, u);
         if (!it.ok) continue;
+        if (!ctl.wait(LB_Q_FULL, n & 1u)) break;
+        ++n;
         int kt = lnext_tile(a, it, it.kt0 - 1);
-        if (kt >= it.kt1) continue;
+        if (kt >= it.kt1) {
+          ptx::tc_commit(ctl.bar(LB_Q_EMPTY));
+          continue;
+        }
         bool first = true;
         const uint32_t sP = sbase + kLOffP;
         for (;;) {
           const int kn = lnext_tile(a, it, kt);
+          // S^T of latent panels 4..7 into its own accumulator (the softmax adds the two)
+          for (int pn = kLQkSplit; pn < kLPanels - 1 && !stop; ++pn) {
+            if (!ctl.wait(LB_SLOT_FULL + pn, g & 1u)) {
+              stop = true;
+              break;
+            }
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              ptx::mma_ss(tmem + kLColS2, ptx::smem_desc(sK + pn * kLKPanel + ks * 32, 16, 1024),
+                          ptx::smem_desc(sQ + pn * kLQPanel + ks * 32, 16, 1024), kLIdQK,
+                          (pn != kLQkSplit || ks != 0) ? 1u : 0u);
+          }
+          if (stop) break;
+          ptx::tc_commit(ctl.bar(LB_S_FULL));
+          if (kn >= it.kt1) ptx::tc_commit(ctl.bar(LB_Q_EMPTY));
           if (!ctl.wait(LB_P_LO, g & 1u)) {
             stop = true;
             break;
@@ -683,8 +707,12 @@ __global__ void __launch_bounds__(kLThreads, 1)
         uint32_t flags = 0;
         if (ok) {
           ptx::tc_fence_after();
+          float x2[32];
           ptx::tmem_ld32(tmem + lane_off + kLColS + 32u * hf, reinterpret_cast<uint32_t*>(x));
+          ptx::tmem_ld32(tmem + lane_off + kLColS2 + 32u * hf, reinterpret_cast<uint32_t*>(x2));
           ptx::tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) x[c] += x2[c];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             x[c] = (vmask >> c) & 1u ? x[c] * c2 : -INFINITY;
